@@ -314,9 +314,11 @@ static uint8_t e4m3_round_magnitude(double a) {
   return (lo & 1) ? (uint8_t)hi : (uint8_t)lo;  // tie -> even mantissa LSB
 }
 
+// Sign-magnitude encoding: the sign bit follows the input's sign, also when
+// the magnitude rounds to zero (IEEE-style rounding keeps the sign of zero).
 uint8_t oracle_e4m3_encode(double v) {
   const uint8_t mag = e4m3_round_magnitude(std::fabs(v));
-  return (v < 0 && mag != 0) ? (uint8_t)(mag | 0x80) : mag;
+  return std::signbit(v) ? (uint8_t)(mag | 0x80) : mag;
 }
 
 // Quantise one block of n values (n <= 32) in place of the MX rule above.
