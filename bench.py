@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the sigmoid-routed top-k MoE FFN layer (forward) on GB300.
+
+One step = one whole layer call (routing, permutation, grouped SwiGLU GEMMs,
+combine, shared expert on its own stream) on one batch of synthetic inputs
+that are already resident in HBM. Default workload: the Hy3-shape decode
+layer (T=64 tokens, H=4096, E=192 routed experts, top-8, I=1536, one shared
+expert of I=1536, bf16 weights ~N(0, 0.02)).
+
+Prints ONE JSON line (rank 0). Multi-GPU (torchrun): every rank runs its own
+replica on its own tokens (no collective on the data path); `value` is the
+tokens of all ranks divided by the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny]
+  python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE-layer tokens/sec at Hy3 shape; achieved HBM GB/s (decode) and TFLOP/s (prefill) vs peak")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of the routed GEMM-1 kernel per launch at the decode workload,
+# from the ncu capture summarised in profiles/ (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only for the gemm.cu it was taken on.
+GEMM1_TRAFFIC = {"gemm_cu_sha": None, "bytes": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_max(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        import torch
+
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.device_index).uuid)
+        except Exception:
+            uuid = str(self.device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100", "-i", uuid],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+def algorithmic_work(shape, counts):
+    """Bytes the layer must move and FLOPs it must do, from the expert counts."""
+    H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
+    touched = int((counts > 0).sum())
+    w_expert = 3 * H * I * 2
+    w_shared = 3 * H * Is * 2
+    layer_bytes = touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2
+    flops = 6 * H * I * T * K + 6 * H * Is * T
+    TK = T * K
+    gemm1_bytes = touched * 2 * I * H * 2 + TK * H * 2 + TK * I * 2
+    return dict(touched=touched, layer_bytes=layer_bytes, flops=flops, gemm1_bytes=gemm1_bytes,
+                gemm1_flops=4 * H * I * TK)
+
+
+def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None = None):
+    """Time the oracle on a bounded sample of tokens; returns (tokens/s, n, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+
+    xh = x.cpu()
+    lh = logits.cpu()
+    wh = {k: v.cpu() for k, v in w.items()}
+    args = [wh[k] for k in ("w_gate", "w_up", "w_down")]
+    if shape.I_shared:
+        args += [wh[k] for k in ("ws_gate", "ws_up", "ws_down")]
+    # Convert once, outside the timed calls.
+    import oracle as _o
+    conv = [_o._bf16_bits(a) for a in args]
+    xb = _o._bf16_bits(xh)
+    t0 = time.perf_counter()
+    oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
+                         tokens=np.array([0], np.int32))
+    t1 = time.perf_counter() - t0
+    n = max(1, int(budget_s / max(t1, 1e-6)))
+    n = min(n, shape.T if max_tokens is None else max_tokens)
+    toks = (np.arange(n) % shape.T).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
+                         tokens=toks)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt, oracle.num_threads()
+
+
+def gemm_cu_sha():
+    p = os.path.join(ROOT, "routed_expert_ffn_04_gb300", "csrc", "gemm.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import routed_expert_ffn_04_gb300 as moe
+    import synth
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shape = synth.WORKLOADS[args.workload]
+    moe.load()  # fails loudly when the library is not built
+
+    x, logits = synth.make_activations(shape, device=dev, seed=rank)
+    w = synth.make_weights(shape, device=dev, seed=0)
+    layer = moe.MoELayer(shape, w, device=local)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    main = torch.cuda.current_stream(dev)
+
+    # Routing counts of this input (for the algorithmic bytes), outside timing.
+    cfg = layer.cfg
+    idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device=dev)
+    tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device=dev)
+    moe.route(layer.handle, cfg, logits, idx, tw)
+    counts = torch.bincount(idx.flatten().long(), minlength=shape.E).cpu().numpy()
+    work = algorithmic_work(shape, counts)
+
+    for _ in range(args.warmup):
+        layer(x, logits, out)
+    torch.cuda.synchronize()
+    layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(main)
+    for _ in range(args.steps):
+        layer(x, logits, out)
+    ev1.record(main)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = dist_max(ms, world, dev)
+    stage_ms, n_calls = layer.handle.stage_times()
+    layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
+    status = layer.handle.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} during the timed region")
+
+    # End-to-end through the host entry point: pinned host x/logits in, out back.
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    oh = torch.empty((shape.T, shape.H), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    for _ in range(3):
+        moe.layer_forward_host(layer.handle, cfg, layer.weights, xh, lh, oh, layer.ws, side=layer.side)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        moe.layer_forward_host(layer.handle, cfg, layer.weights, xh, lh, oh, layer.ws, side=layer.side)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e_ms = dist_max(e2e_ms, world, dev)
+
+    peaks, peak_src = load_peaks()
+    g1_ms = stage_ms["gemm_gate_up"]
+    bound = "hbm" if args.workload in ("decode", "tiny") else "tensor"
+    if bound == "hbm":
+        achieved = work["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        unit = "GB/s"
+    else:
+        achieved = work["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        unit = "TFLOP/s"
+    traffic = GEMM1_TRAFFIC["bytes"] if (GEMM1_TRAFFIC["gemm_cu_sha"] == gemm_cu_sha()
+                                         and args.workload == "decode") else None
+    value = shape.T * world / (ms * 1e-3)
+    layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
+    layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
+    launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
+        "config": {
+            "workload": f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer",
+            "T": shape.T, "H": shape.H, "E": shape.E, "K": shape.K, "I": shape.I, "I_shared": shape.I_shared,
+            "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
+            "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "kernel": "routed grouped GEMM-1 (gate/up + SwiGLU)",
+            "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes": work["gemm1_bytes"], "avg_launch_ms": round(g1_ms, 5),
+            "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})",
+            "launches_timed": n_calls,
+        },
+        "layer": {
+            "touched_experts": work["touched"], "algorithmic_bytes": work["layer_bytes"], "flops": work["flops"],
+            "achieved_gbs": round(layer_gbs, 1), "hbm_frac": round(layer_gbs / float(peaks["hbm_gbs"]), 4),
+            "achieved_tflops": round(layer_tflops, 2),
+            "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        },
+        "e2e": {"value": round(shape.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": shape.T * shape.H * 2 + shape.T * shape.E * 4,
+                "d2h_bytes_per_step": shape.T * shape.H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, n, dt, thr = cpu_oracle_rate(shape, x, logits, w, budget_s=12.0)
+        result["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                  "sample": f"{n} tokens of the {args.workload} workload through the fp64 oracle "
+                                            f"({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    x, logits = synth.make_activations(shape, device=dev, seed=0)
+    w = synth.make_weights(shape, device=dev, seed=0)
+    keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if shape.I_shared else [])
+    conv = [oracle._bf16_bits(w[k]) for k in keys]
+    xb = oracle._bf16_bits(x)
+    lh = logits.cpu().numpy()
+    del w
+
+    def step(n):
+        toks = (np.arange(n) % shape.T).astype(np.int32)
+        oracle.layer_forward(xb, lh, *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
+                             tokens=toks)
+
+    t0 = time.perf_counter()
+    step(1)
+    t1 = time.perf_counter() - t0
+    total_budget = 150.0  # seconds for warmup + timed steps
+    n = max(1, min(shape.T, int(total_budget / max(1, args.steps + args.warmup) / max(t1, 1e-6))))
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    value = n / (ms * 1e-3)
+    thr = oracle.num_threads()
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeds as the CUDA arm)",
+        "config": {"workload": f"Hy3-shape {args.workload} MoE layer", "T": shape.T, "H": shape.H, "E": shape.E,
+                   "K": shape.K, "I": shape.I, "I_shared": shape.I_shared},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": f"{n} token(s) of the {args.workload} workload per step through the fp64 oracle"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,263 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) sigmoid-routed top-k MoE FFN layer.
+ *
+ * The layer (forward pass) is the MoE block of the Hy3 / Hy4 /
+ * HunyuanImage-3.0 models:
+ *   out[t] = sum_k w[t,k] * FFN_{e(t,k)}(x[t]) + FFN_shared(x[t])
+ * with FFN(x) = W_down (silu(W_gate x) * (W_up x)) and (e, w) from sigmoid
+ * top-k routing with route_norm and router_scaling_factor.
+ *
+ * Passages that define it (page titles):
+ *   [Hy3]  "腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战"
+ *          section 一: 192 routed experts, top-8 sigmoid routing, 1 shared
+ *          expert, expert intermediate 1536, hidden 4096,
+ *          router_scaling_factor=2.826, route_norm=True.
+ *          section 8.5: the main stream runs gating, then the routed path
+ *          (InitRouting -> grouped GMM -> FinalizeRouting), then the combine
+ *          add; the shared expert runs on a second stream that starts after
+ *          gating and is joined before the add.
+ *          section 8.2: routed and shared Linears in W8A8 MXFP8.
+ *   [HyI3] "HunyuanImage-3.0 MoE 多流变体实战", 源码级实现拆解 §1-§3:
+ *          a side stream created once and passed in; input_ready_event
+ *          recorded on the main stream and waited on by the side stream;
+ *          mlp_done_event recorded on the side stream and waited on by the
+ *          main stream; output = hidden_states_mlp + combined_output.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device pointers; the caller owns all
+ *     buffers. No entry point allocates device memory per call; scratch comes
+ *     from a caller-provided workspace whose size the *_workspace_size calls
+ *     return. moe_create allocates a 64-byte device status word once.
+ *   - Every device pointer must be 16-byte aligned (MOE_ERR_INVALID_ARG).
+ *   - Matrices are dense row-major. Weights are K-major: the reduction axis
+ *     is the last (contiguous) one.
+ *   - Calls are asynchronous on the given stream(s) and never synchronise
+ *     the host, except moe_get_device_status, moe_read_stage_times and
+ *     moe_layer_forward_host, which say so.
+ *   - Argument errors are returned before any launch. A failed launch
+ *     returns MOE_ERR_CUDA. A device-side wait that gives up (a bounded
+ *     spin, about 2 s) records a code in the handle's status word, which
+ *     moe_get_device_status reports; outputs of that call are undefined.
+ *   - A handle is bound to one device and is not thread-safe; use one
+ *     handle per concurrently used stream pair.
+ *   - Streams are cudaStream_t values passed as void*; NULL is the legacy
+ *     default stream.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_API __attribute__((visibility("default")))
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or config */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  MOE_ERR_WORKSPACE = 3,     /* workspace smaller than *_workspace_size */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5 /* a device-side bounded wait gave up */
+} moe_status_t;
+
+typedef enum {
+  MOE_BF16 = 0,       /* bf16 operands, fp32 accumulation */
+  MOE_MXFP8_E4M3 = 1  /* E4M3 elements + one E8M0 scale per 32 along K */
+} moe_dtype_t;
+
+/* Layer shape. T tokens, H hidden, E routed experts, K experts per token,
+ * I routed-expert intermediate size, I_shared shared-expert intermediate size
+ * (0 = no shared expert). scaling = router_scaling_factor ([Hy3] section 一:
+ * 2.826); route_norm != 0 divides the K sigmoid scores by their sum.
+ * Limits: 1 <= K <= min(E, 32), E <= 1024, H % 64 == 0, I % 64 == 0,
+ * I_shared % 64 == 0, T * K < 2^31, T*max(H,I) < 2^31. */
+typedef struct {
+  int T, H, E, K, I, I_shared;
+  float scaling;
+  int route_norm;
+  moe_dtype_t dtype;
+} moe_config_t;
+
+/* Layer weights (device). bf16 mode: w_* are bf16, s_* ignored.
+ * MXFP8 mode: w_* are E4M3 codes (uint8) and s_* the E8M0 scales, one per
+ * 32 consecutive elements of a row ([rows, cols/32]).
+ *   w_gate, w_up: [E, I, H]     w_down: [E, H, I]
+ *   ws_gate, ws_up: [I_shared, H]   ws_down: [H, I_shared]  (NULL if I_shared == 0) */
+typedef struct {
+  const void *w_gate, *w_up, *w_down;
+  const uint8_t *s_gate, *s_up, *s_down;
+  const void *ws_gate, *ws_up, *ws_down;
+  const uint8_t *ss_gate, *ss_up, *ss_down;
+} moe_weights_t;
+
+typedef struct moe_handle* moe_handle_t;
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+/* Options for moe_set_option. */
+typedef enum {
+  /* Grouped GEMM tiling: 0 = automatic (default), 1 = weight rows fill the
+   * 128-row MMA tile and tokens form N (small token counts per expert),
+   * 2 = tokens fill the 128-row MMA tile (large token counts per expert). */
+  MOE_OPT_GEMM_MODE = 0,
+  /* 1 = record CUDA events between the stages of moe_layer_forward so
+   * moe_read_stage_times can report per-stage device time. Default 0. */
+  MOE_OPT_STAGE_TIMING = 1,
+  /* Device wait limit in microseconds for bounded spins (default 2000000). */
+  MOE_OPT_WAIT_LIMIT_US = 2
+} moe_option_t;
+
+/* Stage indices reported by moe_read_stage_times. */
+enum {
+  MOE_STAGE_ROUTE = 0,        /* sigmoid top-k routing kernel            */
+  MOE_STAGE_PERMUTE = 1,      /* histogram, scan, scatter, row gather    */
+  MOE_STAGE_GEMM_GATE_UP = 2, /* routed grouped GEMM-1 + SwiGLU epilogue */
+  MOE_STAGE_GEMM_DOWN = 3,    /* routed grouped GEMM-2                   */
+  MOE_STAGE_COMBINE = 4,      /* join with the shared stream + combine   */
+  MOE_STAGE_SHARED = 5,       /* shared expert on its stream             */
+  MOE_STAGE_TOTAL = 6,        /* whole call on the main stream           */
+  MOE_NUM_STAGES = 7
+};
+
+/* Create a handle on `device`: records the SM count, resolves the TMA
+ * descriptor encoder, allocates the device status word and two events.
+ * Returns MOE_ERR_CUDA if the device is unusable. */
+MOE_API moe_status_t moe_create(int device, moe_handle_t* out);
+MOE_API moe_status_t moe_destroy(moe_handle_t h);
+MOE_API const char* moe_status_string(moe_status_t s);
+MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value);
+
+/* Workspace bytes moe_layer_forward / moe_layer_forward_host need for cfg
+ * (host-only, no GPU needed). */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Step 1, routing ([Hy3] section 一; the gating result is the input).
+ * logits (device): [T, E] fp32. Per token, the K experts with the largest
+ * fp32 logits, in descending logit order, equal logits -> lower id first
+ * (+0 and -0 are equal; NaN ranks below every number).
+ * topk_w[t,k] = scaling * sigma(l_k) / (route_norm ? sum_j sigma(l_j) : 1).
+ * topk_idx (device): [T, K] int32 out. topk_w (device): [T, K] fp32 out. */
+MOE_API moe_status_t moe_route(moe_handle_t h, const moe_config_t* cfg, const float* logits,
+                               int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/* Scratch bytes moe_permute needs (host-only). */
+MOE_API moe_status_t moe_permute_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Step 2, InitRouting ([Hy3] sections 8.1, 8.5): stable counting sort of the
+ * T*K (token, slot) pairs (flat index f = t*K + k) by expert id, then a row
+ * gather. Outputs (device): counts [E], offsets [E+1] (exclusive scan),
+ * perm_src [T*K] (permuted row -> f), flat_to_perm [T*K] (its inverse),
+ * x_perm [T*K, H] = x[perm_src[r] / K]. Rows of one expert keep ascending f.
+ * x (device): [T, H] bf16; MXFP8 mode: E4M3 codes with x_scale [T, H/32]
+ * and x_perm_scale [T*K, H/32] (else both ignored). An expert id outside
+ * [0, E) is skipped and recorded in the device status word. */
+MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const void* x,
+                                 const uint8_t* x_scale, const int32_t* topk_idx, int32_t* counts,
+                                 int32_t* offsets, int32_t* perm_src, int32_t* flat_to_perm,
+                                 void* x_perm, uint8_t* x_perm_scale, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+
+/* Scratch bytes moe_grouped_swiglu_gemm needs: the [rows, I] intermediate. */
+MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int I, moe_dtype_t dtype,
+                                                     size_t* bytes);
+
+/* Step 3, the grouped expert GEMM with SwiGLU (the grouped GMM of [Hy3]
+ * section 8.5): for each group g, rows offsets[g] .. offsets[g+1]-1 of `a`:
+ *   h = silu(a W_gate[g]^T) * (a W_up[g]^T)   (fp32 accumulate, h stored bf16
+ *                                              or, in MXFP8 mode, re-quantised)
+ *   y = h W_down[g]^T                          (fp32 accumulate, stored fp32)
+ * a (device): [rows, H] bf16 (MXFP8: E4M3 + a_scale [rows, H/32]).
+ * offsets (device): [num_groups + 1] int32, non-decreasing, offsets[0] = 0,
+ *   offsets[num_groups] <= rows; NULL means one group of all rows (a dense
+ *   SwiGLU MLP, used for the shared expert).
+ * w_gate, w_up: [num_groups, I, H]; w_down: [num_groups, H, I] (device).
+ * y (device): [rows, H] fp32 out; rows outside every group are not written.
+ * Limits: num_groups <= 1024, H % 64 == 0, I % 64 == 0. */
+MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int rows, int H,
+                                             int I, moe_dtype_t dtype, const void* a,
+                                             const uint8_t* a_scale, const int32_t* offsets,
+                                             const void* w_gate, const void* w_up,
+                                             const void* w_down, const uint8_t* s_gate,
+                                             const uint8_t* s_up, const uint8_t* s_down, float* y,
+                                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 4, FinalizeRouting + shared add ([Hy3] section 8.5 "combine 相加";
+ * [HyI3] §3 output = hidden_states_mlp + combined_output):
+ *   out[t] = bf16_rne( sum_{k=0..K-1} topk_w[t,k] * y_perm[flat_to_perm[t*K+k]]
+ *                      + shared_out[t] )
+ * summed in fp32 in that order and rounded once.
+ * y_perm (device): [T*K, H] fp32; topk_w: [T, K] fp32; flat_to_perm: [T*K];
+ * shared_out (device, nullable): [T, H] fp32; out (device): [T, H] bf16. */
+MOE_API moe_status_t moe_combine(moe_handle_t h, const moe_config_t* cfg, const float* y_perm,
+                                 const float* topk_w, const int32_t* flat_to_perm,
+                                 const float* shared_out, void* out, moe_stream_t stream);
+
+/* MXFP8 quantisation of a bf16 matrix along its rows (npu_dynamic_mx_quant in
+ * [Hy3] section 六; rule of the OCP MX v1.0 spec): per block of 32, scale
+ * X = 2^(floor(log2 amax) - 8) stored as E8M0, elements RNE(v / X) to E4M3
+ * saturating at +-448; an all-zero block gets scale code 0.
+ * in (device): [rows, cols] bf16; q (device): [rows, cols] uint8 out;
+ * scale (device): [rows, cols/32] uint8 out. cols % 32 == 0. */
+MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int64_t rows,
+                                        int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream);
+
+/* The whole layer, steps 1-4 plus the shared expert, with the two-stream
+ * orchestration of [Hy3] section 8.5 / [HyI3] §3: an event recorded on
+ * `main` at entry is waited on by `side`, which runs the shared expert and
+ * records a second event that `main` waits on before the combine.
+ * side == NULL runs the shared expert on `main` before the routed path.
+ * x (device): [T, H] bf16 (MXFP8 mode: quantised inside, per call).
+ * logits (device): [T, E] fp32. out (device): [T, H] bf16.
+ * ws (device): at least moe_workspace_size bytes. */
+MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
+                                       const moe_weights_t* w, const void* x, const float* logits,
+                                       void* out, void* ws, size_t ws_bytes, moe_stream_t main,
+                                       moe_stream_t side);
+
+/* The same layer with HOST activations: copies x_host [T, H] bf16 and
+ * logits_host [T, E] fp32 to the device (staging inside ws), runs
+ * moe_layer_forward, copies out back to out_host [T, H] bf16 and
+ * synchronises `main`. Weights stay device-resident. Host buffers should be
+ * pinned for asynchronous copies. */
+MOE_API moe_status_t moe_layer_forward_host(moe_handle_t h, const moe_config_t* cfg,
+                                            const moe_weights_t* w, const void* x_host,
+                                            const float* logits_host, void* out_host, void* ws,
+                                            size_t ws_bytes, moe_stream_t main, moe_stream_t side);
+
+/* Read and clear the handle's device status word (synchronises `stream`).
+ * *code = 0 when no device-side error was recorded since the last read;
+ * otherwise the code of the first failure (see the MOE_DEV_* values below)
+ * and the call returns MOE_ERR_DEVICE_TIMEOUT for wait timeouts or
+ * MOE_ERR_INVALID_ARG for bad expert ids / permutation indices. */
+MOE_API moe_status_t moe_get_device_status(moe_handle_t h, int* code, moe_stream_t stream);
+
+enum {
+  MOE_DEV_OK = 0,
+  MOE_DEV_TIMEOUT_PRODUCER = 1, /* GEMM TMA producer gave up waiting */
+  MOE_DEV_TIMEOUT_MMA = 2,      /* GEMM MMA issuer gave up waiting */
+  MOE_DEV_TIMEOUT_EPILOGUE = 3, /* GEMM epilogue gave up waiting */
+  MOE_DEV_TIMEOUT_SELFTEST = 4, /* moe_selftest_wait_timeout's wait */
+  MOE_DEV_BAD_EXPERT_ID = 16,   /* moe_permute saw an id outside [0, E) */
+  MOE_DEV_BAD_PERM_INDEX = 17   /* a permutation index out of range */
+};
+
+/* Average device time per stage (ms) over the last calls of
+ * moe_layer_forward made with MOE_OPT_STAGE_TIMING on (at most 512; the
+ * window restarts after each read). ms: MOE_NUM_STAGES floats out (-1 for a
+ * stage that did not run). *n_calls: calls averaged. Synchronises the
+ * recorded events. */
+MOE_API moe_status_t moe_read_stage_times(moe_handle_t h, float* ms, int* n_calls);
+
+/* Launch one block whose thread waits on an mbarrier that nothing ever
+ * arrives on, with the handle's wait limit; the wait gives up, records
+ * MOE_DEV_TIMEOUT_SELFTEST in the status word and the kernel returns. Used to
+ * test the bounded-wait path without hanging the GPU. */
+MOE_API moe_status_t moe_selftest_wait_timeout(moe_handle_t h, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,263 @@
+"""Python binding of the GB300 MoE FFN layer library (libmoe_gb300.so).
+
+Argument marshalling only: every step runs in the CUDA kernels behind the C
+ABI of include/moe.h. PyTorch provides device memory and streams. The binding
+refuses to run when the compiled library is missing; there is no CPU path.
+
+Names follow the C ABI: route, permute, grouped_swiglu_gemm, combine,
+quantize_mxfp8, layer_forward, layer_forward_host.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import _build
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = _build.LIB
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = range(6)
+MOE_BF16, MOE_MXFP8_E4M3 = 0, 1
+MOE_OPT_GEMM_MODE, MOE_OPT_STAGE_TIMING, MOE_OPT_WAIT_LIMIT_US = 0, 1, 2
+STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine", "shared", "total"]
+DEV_TIMEOUT_SELFTEST = 4
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("K", ctypes.c_int),
+                ("I", ctypes.c_int), ("I_shared", ctypes.c_int), ("scaling", ctypes.c_float),
+                ("route_norm", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
+                 "ws_gate", "ws_up", "ws_down", "ss_gate", "ss_up", "ss_down")]
+
+
+def exported_names() -> list[str]:
+    """Entry points declared in include/moe.h (MOE_API functions)."""
+    text = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def load(build_if_missing: bool = False):
+    """Load the compiled library; raise if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        if build_if_missing:
+            _build.build()
+        else:
+            raise ImportError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    PS = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "moe_create": [I, ctypes.POINTER(P)],
+        "moe_destroy": [P],
+        "moe_set_option": [P, I, I],
+        "moe_workspace_size": [P, PS],
+        "moe_route": [P, P, P, P, P, P],
+        "moe_permute_workspace_size": [P, PS],
+        "moe_permute": [P, P, P, P, P, P, P, P, P, P, P, P, S, P],
+        "moe_grouped_gemm_workspace_size": [I, I, I, PS],
+        "moe_grouped_swiglu_gemm": [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, S, P],
+        "moe_combine": [P, P, P, P, P, P, P, P],
+        "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
+        "moe_layer_forward": [P, P, P, P, P, P, P, S, P, P],
+        "moe_layer_forward_host": [P, P, P, P, P, P, P, S, P, P],
+        "moe_get_device_status": [P, ctypes.POINTER(I), P],
+        "moe_read_stage_times": [P, ctypes.POINTER(F), ctypes.POINTER(I)],
+        "moe_selftest_wait_timeout": [P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = I
+    lib.moe_status_string.argtypes = [I]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    return load().moe_status_string(int(s)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoEError(rc, what)
+
+
+def _p(t):
+    """Device/host pointer of a tensor (None -> NULL)."""
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_config(T, H, E, K, I, I_shared, scaling, route_norm=True, dtype=MOE_BF16) -> Config:
+    return Config(int(T), int(H), int(E), int(K), int(I), int(I_shared), float(scaling), int(bool(route_norm)), int(dtype))
+
+
+def workspace_size(cfg: Config) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def permute_workspace_size(cfg: Config) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_permute_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_permute_workspace_size")
+    return n.value
+
+
+def grouped_gemm_workspace_size(rows: int, I: int, dtype: int = MOE_BF16) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_grouped_gemm_workspace_size(int(rows), int(I), int(dtype), ctypes.byref(n)),
+           "moe_grouped_gemm_workspace_size")
+    return n.value
+
+
+class Handle:
+    """Owns a moe_handle_t (device, SM count, status word, events)."""
+
+    def __init__(self, device: int | None = None):
+        lib = load()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = int(device)
+        h = ctypes.c_void_p()
+        _check(lib.moe_create(self.device, ctypes.byref(h)), "moe_create")
+        self._h = h
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            load().moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, opt: int, value: int):
+        _check(load().moe_set_option(self._h, int(opt), int(value)), "moe_set_option")
+
+    def device_status(self, stream=None) -> int:
+        code = ctypes.c_int(0)
+        rc = load().moe_get_device_status(self._h, ctypes.byref(code), _stream(stream))
+        if rc not in (MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_INVALID_ARG):
+            _check(rc, "moe_get_device_status")
+        return code.value
+
+    def stage_times(self) -> tuple[dict, int]:
+        ms = (ctypes.c_float * 7)()
+        n = ctypes.c_int(0)
+        _check(load().moe_read_stage_times(self._h, ms, ctypes.byref(n)), "moe_read_stage_times")
+        return {k: ms[i] for i, k in enumerate(STAGES)}, n.value
+
+    def selftest_wait_timeout(self, stream=None):
+        _check(load().moe_selftest_wait_timeout(self._h, _stream(stream)), "moe_selftest_wait_timeout")
+
+
+def route(h: Handle, cfg: Config, logits, topk_idx, topk_w, stream=None):
+    _check(load().moe_route(h.ptr, ctypes.byref(cfg), _p(logits), _p(topk_idx), _p(topk_w), _stream(stream)), "moe_route")
+
+
+def permute(h: Handle, cfg: Config, x, topk_idx, counts, offsets, perm_src, flat_to_perm, x_perm, ws,
+            x_scale=None, x_perm_scale=None, stream=None):
+    _check(load().moe_permute(h.ptr, ctypes.byref(cfg), _p(x), _p(x_scale), _p(topk_idx), _p(counts), _p(offsets),
+                              _p(perm_src), _p(flat_to_perm), _p(x_perm), _p(x_perm_scale), _p(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+
+
+def grouped_swiglu_gemm(h: Handle, a, offsets, w_gate, w_up, w_down, y, ws, *, num_groups: int, H: int, I: int,
+                        dtype: int = MOE_BF16, a_scale=None, s_gate=None, s_up=None, s_down=None, stream=None):
+    rows = a.shape[0]
+    _check(load().moe_grouped_swiglu_gemm(h.ptr, int(num_groups), int(rows), int(H), int(I), int(dtype), _p(a),
+                                          _p(a_scale), _p(offsets), _p(w_gate), _p(w_up), _p(w_down), _p(s_gate),
+                                          _p(s_up), _p(s_down), _p(y), _p(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "moe_grouped_swiglu_gemm")
+
+
+def combine(h: Handle, cfg: Config, y_perm, topk_w, flat_to_perm, shared_out, out, stream=None):
+    _check(load().moe_combine(h.ptr, ctypes.byref(cfg), _p(y_perm), _p(topk_w), _p(flat_to_perm), _p(shared_out),
+                              _p(out), _stream(stream)), "moe_combine")
+
+
+def quantize_mxfp8(h: Handle, x, q, scale, stream=None):
+    rows = x.numel() // x.shape[-1]
+    _check(load().moe_quantize_mxfp8(h.ptr, _p(x), int(rows), int(x.shape[-1]), _p(q), _p(scale), _stream(stream)),
+           "moe_quantize_mxfp8")
+
+
+def make_weights(w: dict) -> Weights:
+    ws = Weights()
+    for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down", "s_gate", "s_up", "s_down",
+              "ss_gate", "ss_up", "ss_down"):
+        t = w.get(k)
+        setattr(ws, k, t.data_ptr() if t is not None else None)
+    return ws
+
+
+def layer_forward(h: Handle, cfg: Config, weights: Weights, x, logits, out, ws, main=None, side=None):
+    side_p = ctypes.c_void_p(side.cuda_stream) if side is not None else None
+    _check(load().moe_layer_forward(h.ptr, ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(logits), _p(out),
+                                    _p(ws), ws.numel() * ws.element_size(), _stream(main), side_p),
+           "moe_layer_forward")
+
+
+def layer_forward_host(h: Handle, cfg: Config, weights: Weights, x_host, logits_host, out_host, ws, main=None,
+                       side=None):
+    side_p = ctypes.c_void_p(side.cuda_stream) if side is not None else None
+    _check(load().moe_layer_forward_host(h.ptr, ctypes.byref(cfg), ctypes.byref(weights), _p(x_host),
+                                         _p(logits_host), _p(out_host), _p(ws), ws.numel() * ws.element_size(),
+                                         _stream(main), side_p), "moe_layer_forward_host")
+
+
+class MoELayer:
+    """Convenience owner of a handle, workspace and side stream for one shape."""
+
+    def __init__(self, shape, weights: dict, device=None, side_stream=True):
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        self.shape = shape
+        self.cfg = make_config(shape.T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.scaling,
+                               shape.route_norm, MOE_MXFP8_E4M3 if shape.dtype == "mxfp8" else MOE_BF16)
+        self.handle = Handle(self.device.index)
+        self.ws = torch.empty(workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
+        self.weights_t = weights
+        self.weights = make_weights(weights)
+        self.side = torch.cuda.Stream(device=self.device) if side_stream else None
+
+    def __call__(self, x, logits, out=None, main=None):
+        if out is None:
+            out = torch.empty((self.shape.T, self.shape.H), dtype=torch.bfloat16, device=self.device)
+        layer_forward(self.handle, self.cfg, self.weights, x, logits, out, self.ws, main=main, side=self.side)
+        return out

@@ -1,0 +1,532 @@
+// Step 3: grouped expert GEMM with the SwiGLU epilogue fused, on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM), operands
+// staged by TMA. This is the "分组 GMM" / FusedMoEGMM step of the routed path
+// ("腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战", section 8.5: the
+// routed path is the bulk of the MoE block's time) with the expert FFN of
+// section 一 (intermediate 1536) in SwiGLU form.
+//
+//   GEMM-1 (MODE 0):  h[r, i] = silu(sum_c a[r,c] Wg[g,i,c]) * (sum_c a[r,c] Wu[g,i,c])
+//   GEMM-2 (MODE 1):  y[r, m] = sum_i h[r,i] Wd[g,m,i]
+// for every row r of group g (rows offsets[g] .. offsets[g+1]-1).
+//
+// Kernel structure (persistent, one CTA per SM, 192 threads):
+//   warp 0      TMA producer (one thread): fills a ring of shared-memory
+//               stages, each one K-slice of 64 elements of both operands.
+//   warp 1      TMEM allocator + MMA issuer (one thread): tcgen05.mma into a
+//               double-buffered TMEM accumulator, tcgen05.commit frees stages.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator, SwiGLU / fp32 store.
+// Tiles are listed per group on the device (no host read of the group sizes)
+// and dealt to CTAs round-robin.
+//
+// Two tilings (SWAP template flag):
+//   SWAP = true   weights are the 128-row MMA operand A (two A tiles: gate and
+//                 up rows, or two 128-row blocks of W_down) and BN = 32 tokens
+//                 of the group form N. For few tokens per expert (decode) the
+//                 kernel is a weight stream and the MMA barely costs anything.
+//   SWAP = false  128 tokens form A and 256 weight rows form B with N = 256
+//                 (gate 128 + up 128 for GEMM-1), the compute-bound tiling.
+//
+// Every wait is bounded (about 2 s); on expiry the CTA records an error code
+// in the status word, drains its in-flight copies/MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBK = 64;            // K elements per stage = one 128-byte swizzle row
+constexpr int kThreads = 192;      // 6 warps
+constexpr int kMaxGroups = 1024;
+constexpr int kMaxSmem = 232448;   // 227 KB dynamic shared memory per CTA
+
+template <bool SWAP, int MODE, int BN>
+struct Geo {
+  static constexpr int kTileBytes = 128 * 128;                       // 128 rows x 128 B
+  static constexpr int A_BYTES = SWAP ? 2 * kTileBytes : kTileBytes;
+  static constexpr int B_BYTES = SWAP ? BN * 128 : 2 * kTileBytes;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACT_ROWS = SWAP ? BN : 128;                   // activation rows / tile
+  static constexpr int W_COLS = (MODE == 0) ? 128 : 256;             // output cols / tile
+  static constexpr int ACC_COLS = SWAP ? 2 * BN : 256;               // TMEM cols / buffer
+  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32) ? 32 : (2 * ACC_COLS <= 64) ? 64
+                                   : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
+  static constexpr int TABLE_BYTES = (kMaxGroups + 8) * 4;
+  static constexpr int EXTRA = 1024 + TABLE_BYTES + 256;             // align slack + table + bars
+  static constexpr int STAGES_RAW = (kMaxSmem - EXTRA) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TABLE_BYTES + 256;
+  static_assert(STAGES >= 2, "shared memory too small for two stages");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(SMEM <= kMaxSmem, "shared memory budget");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "barrier area");
+  static_assert(!SWAP || (BN % 32 == 0 && BN >= 32 && BN <= 128), "token tile");
+};
+
+struct KParams {
+  const int32_t* offsets;  // [G+1] or nullptr
+  int G;
+  int rows;
+  int num_kb;    // ceil(Kdim / 64)
+  int N;         // output columns per group (I for MODE 0, H for MODE 1)
+  void* out;     // bf16 h (MODE 0) or fp32 y (MODE 1)
+  int* status;
+  uint64_t limit_ns;
+};
+
+struct TileInfo {
+  int g, row0, nrows, wt, tt;
+};
+
+// Group rows [row0, row0 + nrows), clamped to [0, rows).
+__device__ __forceinline__ void group_rows(const KParams& p, int g, int& row0, int& nrows) {
+  if (p.offsets == nullptr) {
+    row0 = 0;
+    nrows = p.rows;
+    return;
+  }
+  int a = __ldg(p.offsets + g), b = __ldg(p.offsets + g + 1);
+  a = a < 0 ? 0 : (a > p.rows ? p.rows : a);
+  b = b < a ? a : (b > p.rows ? p.rows : b);
+  row0 = a;
+  nrows = b - a;
+}
+
+template <int ACT_ROWS, int W_COLS>
+__device__ __forceinline__ TileInfo decode_tile(const KParams& p, const int32_t* tile_start,
+                                                int tile) {
+  int lo = 0, hi = p.G;  // tile_start[lo] <= tile < tile_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo t;
+  t.g = lo;
+  group_rows(p, lo, t.row0, t.nrows);
+  const int n_tt = (t.nrows + ACT_ROWS - 1) / ACT_ROWS;
+  const int local = tile - tile_start[lo];
+  t.wt = local / n_tt;
+  t.tt = local - t.wt * n_tt;
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Bounded wait that ignores the abort flag, used only to drain in-flight work.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) break;
+  }
+}
+
+template <bool SWAP, int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
+                        const __grid_constant__ CUtensorMap map_w0,
+                        const __grid_constant__ CUtensorMap map_w1, const KParams p) {
+  using Gm = Geo<SWAP, MODE, BN>;
+  constexpr int S = Gm::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+  uint8_t* base = smem_raw + pad;
+  const uint32_t stage0 = raw_addr + pad;
+  int32_t* tile_start = reinterpret_cast<int32_t*>(base + S * Gm::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + S * Gm::STAGE_BYTES + Gm::TABLE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- tile table: tile_start[g] = tiles of groups before g.
+  const int n_wt = (p.N + Gm::W_COLS - 1) / Gm::W_COLS;
+  for (int g = threadIdx.x; g < p.G; g += kThreads) {
+    int r0, nr;
+    group_rows(p, g, r0, nr);
+    tile_start[g] = n_wt * ((nr + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Gm::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_act);
+    prefetch_tensormap(&map_w0);
+    prefetch_tensormap(&map_w1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the per-group tile counts
+    const int per = (p.G + 31) / 32;
+    const int b = lane * per;
+    const int e = (b + per < p.G) ? b + per : p.G;
+    int local = 0;
+    for (int g = b; g < e; ++g) local += tile_start[g];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int g = b; g < e; ++g) {
+      const int c = tile_start[g];
+      tile_start[g] = run;
+      run += c;
+    }
+    if (lane == 31) tile_start[p.G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[p.G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_phase = 0;  // bit s: stage s armed / its parity
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<Gm::ACT_ROWS, Gm::W_COLS>(p, tile_start, tile);
+        const int act_row = ti.row0 + ti.tt * Gm::ACT_ROWS;
+        const int w_row0 = ti.g * p.N + ti.wt * Gm::W_COLS;
+        const int w_row1 = (MODE == 0) ? w_row0 : w_row0 + 128;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status,
+                                 MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+          const uint32_t sA = stage0 + stage * Gm::STAGE_BYTES;
+          const uint32_t sB = sA + Gm::A_BYTES;
+          const int kx = kb * kBK;
+          if (SWAP) {
+            tma_load_2d_hint(sA, &map_w0, fb, kx, w_row0, pol_w);
+            tma_load_2d_hint(sA + Gm::kTileBytes, &map_w1, fb, kx, w_row1, pol_w);
+            tma_load_2d(sB, &map_act, fb, kx, act_row);
+          } else {
+            tma_load_2d(sA, &map_act, fb, kx, act_row);
+            tma_load_2d(sB, &map_w0, fb, kx, w_row0);
+            tma_load_2d(sB + Gm::kTileBytes, &map_w1, fb, kx, w_row1);
+          }
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA exits
+        for (int s = 0; s < S; ++s)
+          if (armed & (1u << s)) drain_wait(full_bar(s), (armed_phase >> s) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = SWAP ? idesc_bf16_f32(128, BN) : idesc_bf16_f32(128, 256);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true, issued = false;
+      int local = 0;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t ap = (uint32_t)(local >> 1) & 1u;
+        if (!mbar_wait_bounded(tempty_bar(acc), ap ^ 1u, abort_flag, p.status,
+                               MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * Gm::ACC_COLS);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.status,
+                                 MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = stage0 + stage * Gm::STAGE_BYTES;
+          const uint32_t sB = sA + Gm::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t accum = (kb | k) ? 1u : 0u;
+            const uint64_t bdesc = sw128_kmajor_desc(sB + k * 32);
+            umma_bf16(d, sw128_kmajor_desc(sA + k * 32), bdesc, kIdesc, accum);
+            if (SWAP)
+              umma_bf16(d + BN, sw128_kmajor_desc(sA + Gm::kTileBytes + k * 32), bdesc, kIdesc,
+                        accum);
+          }
+          issued = true;
+          umma_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+      }
+      if (!ok && issued) {  // wait for every issued MMA before TMEM is freed
+        umma_commit(drain_bar);
+        drain_wait(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t ap = (uint32_t)(local >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(tfull_bar(acc), ap, abort_flag, p.status,
+                               MOE_DEV_TIMEOUT_EPILOGUE, p.limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const TileInfo ti = decode_tile<Gm::ACT_ROWS, Gm::W_COLS>(p, tile_start, tile);
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Gm::ACC_COLS);
+      if (SWAP) {
+        // TMEM lane = weight row (output column), TMEM column = token.
+        const int r_first = ti.tt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(tb + c, v0);
+          tmem_ld_32x32b_x32(tb + BN + c, v1);
+          tmem_ld_wait();
+          if (MODE == 0) {
+            const int i = ti.wt * 128 + q * 32 + lane;
+            __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out);
+            if (i < p.N) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int r = r_first + c + j;
+                if (r < ti.nrows) {
+                  const float g = __uint_as_float(v0[j]), u = __uint_as_float(v1[j]);
+                  h[(size_t)(ti.row0 + r) * p.N + i] = __float2bfloat16_rn(silu_f(g) * u);
+                }
+              }
+            }
+          } else {
+            const int m0 = ti.wt * 256 + q * 32 + lane, m1 = m0 + 128;
+            float* y = static_cast<float*>(p.out);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int r = r_first + c + j;
+              if (r < ti.nrows) {
+                float* yr = y + (size_t)(ti.row0 + r) * p.N;
+                if (m0 < p.N) yr[m0] = __uint_as_float(v0[j]);
+                if (m1 < p.N) yr[m1] = __uint_as_float(v1[j]);
+              }
+            }
+          }
+        }
+      } else {
+        // TMEM lane = token row, TMEM column = output column.
+        const int r = ti.tt * 128 + q * 32 + lane;
+        const bool rv = r < ti.nrows;
+        if (MODE == 0) {
+          __nv_bfloat16* hrow =
+              static_cast<__nv_bfloat16*>(p.out) + (size_t)(ti.row0 + (rv ? r : 0)) * p.N;
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tb + c, g);
+            tmem_ld_32x32b_x32(tb + 128 + c, u);
+            tmem_ld_wait();
+            const int col = ti.wt * 128 + c;
+            if (rv && col < p.N) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                const float h1 =
+                    silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                pk[j] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(hrow + col);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+          }
+        } else {
+          float* yrow = static_cast<float*>(p.out) + (size_t)(ti.row0 + (rv ? r : 0)) * p.N;
+#pragma unroll 1
+          for (int c = 0; c < 256; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tb + c, v);
+            tmem_ld_wait();
+            const int col = ti.wt * 256 + c;
+            if (rv && col < p.N) {
+              float4* dst = reinterpret_cast<float4*>(yrow + col);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Gm::TMEM_COLS);
+  }
+}
+
+__global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    // Nothing arrives on this barrier: the wait must give up on its own.
+    mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, MOE_DEV_TIMEOUT_SELFTEST,
+                      limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 2-D bf16 tensor [outer, inner] (inner contiguous), box {64, box_rows},
+// 128-byte swizzle, zero fill out of range.
+bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint32_t box_rows) {
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool SWAP, int MODE, int BN>
+cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
+  using Gm = Geo<SWAP, MODE, BN>;
+  const int Kdim = MODE == 0 ? a.H : a.I;
+  const int N = MODE == 0 ? a.I : a.H;
+  const void* act = MODE == 0 ? a.a : a.h;
+  const void* w0 = MODE == 0 ? a.w_gate : a.w_down;
+  const void* w1 = MODE == 0 ? a.w_up : a.w_down;
+  if (a.rows == 0 || a.G == 0) return cudaSuccess;
+  CUtensorMap m_act, m_w0, m_w1;
+  if (!make_map_bf16(&m_act, act, Kdim, a.rows, Gm::ACT_ROWS) ||
+      !make_map_bf16(&m_w0, w0, Kdim, (uint64_t)a.G * N, 128) ||
+      !make_map_bf16(&m_w1, w1, Kdim, (uint64_t)a.G * N, 128))
+    return cudaErrorInvalidValue;
+  auto kern = grouped_gemm_kernel<SWAP, MODE, BN>;
+  static bool attr_done = false;  // one instantiation per (SWAP, MODE, BN)
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  KParams p;
+  p.offsets = a.offsets;
+  p.G = a.offsets ? a.G : 1;
+  p.rows = a.rows;
+  p.num_kb = (Kdim + kBK - 1) / kBK;
+  p.N = N;
+  p.out = MODE == 0 ? a.h : static_cast<void*>(a.y);
+  p.status = a.status;
+  p.limit_ns = a.wait_limit_ns;
+  const long long n_wt = (N + Gm::W_COLS - 1) / Gm::W_COLS;
+  const long long max_tiles = n_wt * ((a.rows + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS + p.G);
+  const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
+  kern<<<grid, kThreads, Gm::SMEM, s>>>(m_act, m_w0, m_w1, p);
+  return cudaGetLastError();
+}
+
+int pick_mode(const GroupedGemmArgs& a) {
+  if (a.mode == kModeWeightsM || a.mode == kModeTokensM) return a.mode;
+  const int G = a.offsets ? a.G : 1;
+  const double avg_rows = (double)a.rows / (G > 0 ? G : 1);
+  return avg_rows <= 48.0 ? kModeWeightsM : kModeTokensM;
+}
+
+}  // namespace
+
+bool gemm_init_driver() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
+  if (pick_mode(a) == kModeWeightsM) return run_gemm<true, 0, 32>(a, s);
+  return run_gemm<false, 0, 32>(a, s);
+}
+
+cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s) {
+  if (pick_mode(a) == kModeWeightsM) return run_gemm<true, 1, 32>(a, s);
+  return run_gemm<false, 1, 32>(a, s);
+}
+
+cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

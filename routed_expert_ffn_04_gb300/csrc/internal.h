@@ -1,0 +1,65 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Host-side only; nothing here is exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---- routing (route.cu)
+cudaError_t launch_route(const float* logits, int T, int E, int K, float scaling, int route_norm,
+                         int32_t* topk_idx, float* topk_w, cudaStream_t s);
+
+// ---- permutation (permute.cu)
+size_t permute_scratch_bytes(int TK, int E);
+cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* scratch,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                                 int32_t* flat_to_perm, int* status, cudaStream_t s);
+// dst[r, :] = src[perm_src[r] / K, :] for r < TK; rows are row_bytes long
+// (a multiple of 16). A perm_src entry outside [0, TK) gives a zero row.
+cudaError_t launch_gather_rows(const void* src, int src_rows, int row_bytes,
+                               const int32_t* perm_src, int K, int TK, void* dst, int* status,
+                               cudaStream_t s);
+
+// ---- grouped GEMM (gemm.cu)
+enum GemmMode { kModeAuto = 0, kModeWeightsM = 1, kModeTokensM = 2 };
+
+struct GroupedGemmArgs {
+  int G;                   // number of groups
+  const int32_t* offsets;  // [G+1] device, or nullptr: one group of `rows`
+  int rows;                // activation rows
+  int H, I;                // hidden, intermediate
+  const void* a;           // [rows, H] bf16
+  const void* w_gate;      // [G, I, H] bf16
+  const void* w_up;        // [G, I, H] bf16
+  const void* w_down;      // [G, H, I] bf16
+  void* h;                 // [rows, I] bf16 (intermediate)
+  float* y;                // [rows, H] fp32
+  int mode;                // GemmMode
+  int num_sms;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailable
+cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
+
+// ---- combine (combine.cu)
+cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32_t* flat_to_perm,
+                           const float* shared_out, int T, int K, int H, void* out, int* status,
+                           cudaStream_t s);
+
+// ---- MX quantiser (mxquant.cu)
+cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
+                               uint8_t* scale, cudaStream_t s);
+
+// ---- self-test of the bounded wait (gemm.cu)
+cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace moe

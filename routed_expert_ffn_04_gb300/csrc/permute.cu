@@ -1,0 +1,213 @@
+// Step 2: InitRouting — stable expert-contiguous permutation of the T*K
+// (token, slot) pairs and the row gather of the activations.
+// "腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战", section 8.1 (InitRouting
+// matches tokens to experts) and section 8.5 (InitRouting -> grouped GMM ->
+// FinalizeRouting).
+//
+// Counting sort in three kernels, deterministic and without float atomics:
+//   1. hist:    each warp counts expert ids over its chunk of 256 flat
+//               indices (shared-memory counters) -> hist[e][w].
+//   2. scan:    one block turns hist (expert-major) into exclusive bases;
+//               offsets[e] = base[e][0], counts[e] = offsets[e+1]-offsets[e].
+//   3. scatter: each warp walks its chunk in flat order, 32 at a time; lanes
+//               with equal ids are grouped with __match_any_sync and ranked
+//               by lane order, so rows of one expert keep ascending f.
+// A fourth kernel gathers rows with 16-byte vector copies.
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 256;   // flat indices per warp
+constexpr int kWarps = 8;     // warps per block in hist / scatter
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kWarps * 32) perm_hist_kernel(const int32_t* __restrict__ idx,
+                                                                int TK, int E, int NW,
+                                                                int32_t* __restrict__ hist,
+                                                                int* status) {
+  extern __shared__ int32_t sh_hist[];  // [kWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarps + warp;
+  int32_t* h = sh_hist + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (w >= NW) return;
+  for (int p = 0; p < kChunk / 32; ++p) {
+    const int f = w * kChunk + p * 32 + lane;
+    if (f < TK) {
+      const int e = __ldg(idx + f);
+      if ((unsigned)e < (unsigned)E) atomicAdd(h + e, 1);
+      else atomicCAS(status, 0, MOE_DEV_BAD_EXPERT_ID);
+    }
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(size_t)e * NW + w] = h[e];
+}
+
+// Exclusive scan of M = E*NW counts in place (expert-major), by one block.
+__global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* __restrict__ hist, int E,
+                                                                 int NW, int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t grand_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (NW == 0) {  // no (token, slot) pairs: every expert is empty
+    for (int e = tid; e <= E; e += kScanThreads) {
+      offsets[e] = 0;
+      if (e < E) counts[e] = 0;
+    }
+    return;
+  }
+  const long long M = (long long)E * NW;
+  const long long per = (M + kScanThreads - 1) / kScanThreads;
+  const long long b = tid * per;
+  const long long e_ = (b + per < M) ? b + per : M;
+  int32_t local = 0;
+  for (long long i = b; i < e_; ++i) local += hist[i];
+  // Block-wide exclusive scan of `local`.
+  int32_t incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t v = warp_tot[lane];
+    int32_t inc2 = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, inc2, off);
+      if (lane >= off) inc2 += u;
+    }
+    warp_tot[lane] = inc2 - v;  // exclusive prefix of warp totals
+    if (lane == 31) grand_total = inc2;
+  }
+  __syncthreads();
+  int32_t run = warp_tot[warp] + incl - local;
+  for (long long i = b; i < e_; ++i) {
+    const int32_t c = hist[i];
+    hist[i] = run;
+    run += c;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kScanThreads) {
+    const int32_t start = hist[(size_t)e * NW];
+    const int32_t end = (e + 1 < E) ? hist[(size_t)(e + 1) * NW] : grand_total;
+    offsets[e] = start;
+    counts[e] = end - start;
+  }
+  if (tid == 0) offsets[E] = grand_total;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
+    const int32_t* __restrict__ idx, int TK, int E, int NW, const int32_t* __restrict__ base,
+    int32_t* __restrict__ perm_src, int32_t* __restrict__ flat_to_perm) {
+  extern __shared__ int32_t sh_run[];  // [kWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarps + warp;
+  if (w >= NW) return;
+  int32_t* run = sh_run + warp * E;
+  for (int e = lane; e < E; e += 32) run[e] = base[(size_t)e * NW + w];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int p = 0; p < kChunk / 32; ++p) {
+    const int f = w * kChunk + p * 32 + lane;
+    int e = -1;
+    if (f < TK) {
+      e = __ldg(idx + f);
+      if ((unsigned)e >= (unsigned)E) e = -1;
+    }
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(same & lt_mask);
+    const int leader = __ffs(same) - 1;
+    int pos = 0;
+    if (e >= 0) pos = run[e] + rank;
+    __syncwarp();
+    if (e >= 0 && lane == leader) run[e] += __popc(same);
+    __syncwarp();
+    if (e >= 0) {
+      perm_src[pos] = f;
+      flat_to_perm[f] = pos;
+    }
+  }
+}
+
+// One warp per destination row; each lane copies 16-byte vectors, four in flight.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          int src_rows, int vecs,
+                                                          const int32_t* __restrict__ perm_src,
+                                                          int K, int TK, uint4* __restrict__ dst,
+                                                          int* status) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < TK; r += nw) {
+    const int f = __ldg(perm_src + r);
+    const int t = ((unsigned)f < (unsigned)TK) ? f / K : -1;
+    uint4* d = dst + (size_t)r * vecs;
+    if (t < 0 || t >= src_rows) {
+      if (lane == 0) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
+      for (int v = lane; v < vecs; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* s = src + (size_t)t * vecs;
+    int v = lane;
+    for (; v + 96 < vecs; v += 128) {
+      const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64),
+                  a3 = __ldg(s + v + 96);
+      d[v] = a0;
+      d[v + 32] = a1;
+      d[v + 64] = a2;
+      d[v + 96] = a3;
+    }
+    for (; v < vecs; v += 32) d[v] = __ldg(s + v);
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int TK, int E) {
+  const size_t NW = (size_t)(TK + kChunk - 1) / kChunk;
+  return align_up((size_t)E * (NW > 0 ? NW : 1) * sizeof(int32_t), 256);
+}
+
+cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* scratch,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                                 int32_t* flat_to_perm, int* status, cudaStream_t s) {
+  const int NW = (TK + kChunk - 1) / kChunk;
+  int32_t* hist = static_cast<int32_t*>(scratch);
+  const size_t smem = (size_t)kWarps * E * sizeof(int32_t);
+  const int blocks = (NW + kWarps - 1) / kWarps;
+  if (NW > 0) {
+    perm_hist_kernel<<<blocks, kWarps * 32, smem, s>>>(topk_idx, TK, E, NW, hist, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, E, NW, counts, offsets);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || NW == 0) return err;
+  perm_scatter_kernel<<<blocks, kWarps * 32, smem, s>>>(topk_idx, TK, E, NW, hist, perm_src,
+                                                         flat_to_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, int src_rows, int row_bytes,
+                               const int32_t* perm_src, int K, int TK, void* dst, int* status,
+                               cudaStream_t s) {
+  if (TK == 0) return cudaSuccess;
+  const int vecs = row_bytes / 16;
+  long long warps_needed = TK;
+  int blocks = (int)((warps_needed + 7) / 8);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), src_rows, vecs,
+                                            perm_src, K, TK, static_cast<uint4*>(dst), status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
