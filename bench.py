@@ -84,6 +84,12 @@ def dist_max(v: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate(tokens_per_rank: int, ms_local: float, world: int, device) -> tuple[float, float]:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    ms = dist_max(ms_local, world, device)
+    return tokens_per_rank * world / (ms * 1e-3), ms
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -248,8 +254,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms = dist_max(ms, world, dev)
+    value, ms = aggregate(shape.T, ev0.elapsed_time(ev1) / args.steps, world, dev)
     stage_ms, n_calls = layer.handle.stage_times()
     layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
     status = layer.handle.device_status()
@@ -283,7 +288,6 @@ def run_ours(args):
         unit = "TFLOP/s"
     traffic = GEMM1_TRAFFIC["bytes"] if (GEMM1_TRAFFIC["gemm_cu_sha"] == gemm_cu_sha()
                                          and args.workload == "decode") else None
-    value = shape.T * world / (ms * 1e-3)
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1
