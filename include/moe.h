@@ -251,6 +251,33 @@ enum {
  * recorded events. */
 MOE_API moe_status_t moe_read_stage_times(moe_handle_t h, float* ms, int* n_calls);
 
+/* Permutation with no workspace and no allocation (the paper has no
+ * counterpart; this exists for callers of this library that cannot call
+ * cudaMalloc and have no workspace to hand over, such as a plugin inside an
+ * engine that owns every device allocation, or code that must not allocate
+ * after start-up).
+ * Same arguments, results and kernels as moe_permute, minus ws/ws_bytes: the
+ * per-warp histogram lives in a fixed array in the library's own device
+ * memory, MOE_PERMUTE_STATIC_MAX_HIST_INTS int32 (1 MiB), which every GPU
+ * that loads the library holds until the process exits.
+ * Limit: E * ceil(T*K / 256) <= MOE_PERMUTE_STATIC_MAX_HIST_INTS (for E = 192
+ * and K = 8: T <= 43690); larger sizes return MOE_ERR_WORKSPACE before any
+ * launch.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. The call never allocates or frees device memory.
+ * All calls on a device share the one array and each call overwrites it:
+ * calls that overlap on the GPU (different streams, no ordering between
+ * them) race and give undefined results. Nothing in the array needs to
+ * start at zero. */
+#define MOE_PERMUTE_STATIC_MAX_HIST_INTS 262144
+MOE_API moe_status_t moe_permute_static_scratch(moe_handle_t h, const moe_config_t* cfg,
+                                                const void* x, const uint8_t* x_scale,
+                                                const int32_t* topk_idx, int32_t* counts,
+                                                int32_t* offsets, int32_t* perm_src,
+                                                int32_t* flat_to_perm, void* x_perm,
+                                                uint8_t* x_perm_scale, moe_stream_t stream);
+
 /* Launch one block whose thread waits on an mbarrier that nothing ever
  * arrives on, with the handle's wait limit; the wait gives up, records
  * MOE_DEV_TIMEOUT_SELFTEST in the status word and the kernel returns. Used to

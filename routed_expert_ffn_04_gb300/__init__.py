@@ -84,6 +84,7 @@ def load(build_if_missing: bool = False):
         "moe_get_device_status": [P, ctypes.POINTER(I), P],
         "moe_read_stage_times": [P, ctypes.POINTER(F), ctypes.POINTER(I)],
         "moe_selftest_wait_timeout": [P, P],
+        "moe_permute_static_scratch": [P, P, P, P, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -196,6 +197,15 @@ def permute(h: Handle, cfg: Config, x, topk_idx, counts, offsets, perm_src, flat
     _check(load().moe_permute(h.ptr, ctypes.byref(cfg), _p(x), _p(x_scale), _p(topk_idx), _p(counts), _p(offsets),
                               _p(perm_src), _p(flat_to_perm), _p(x_perm), _p(x_perm_scale), _p(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+
+
+def permute_static_scratch(h: Handle, cfg: Config, x, topk_idx, counts, offsets, perm_src, flat_to_perm, x_perm,
+                           x_scale=None, x_perm_scale=None, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate: the
+    histogram lives in a fixed 1 MiB array inside the library (see moe.h)."""
+    _check(load().moe_permute_static_scratch(h.ptr, ctypes.byref(cfg), _p(x), _p(x_scale), _p(topk_idx), _p(counts),
+                                             _p(offsets), _p(perm_src), _p(flat_to_perm), _p(x_perm),
+                                             _p(x_perm_scale), _stream(stream)), "moe_permute_static_scratch")
 
 
 def grouped_swiglu_gemm(h: Handle, a, offsets, w_gate, w_up, w_down, y, ws, *, num_groups: int, H: int, I: int,

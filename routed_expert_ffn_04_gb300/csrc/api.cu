@@ -144,6 +144,11 @@ cudaError_t timing_events(moe_handle_t h) {
 
 }  // namespace
 
+namespace moe {
+int handle_device(moe_handle_t h) { return h->device; }
+int* handle_status_word(moe_handle_t h) { return h->status; }
+}  // namespace moe
+
 extern "C" {
 
 MOE_API const char* moe_status_string(moe_status_t s) {

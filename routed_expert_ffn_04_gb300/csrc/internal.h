@@ -6,7 +6,13 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/moe.h"
+
 namespace moe {
+
+// Handle accessors for translation units other than api.cu.
+int handle_device(moe_handle_t h);
+int* handle_status_word(moe_handle_t h);
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
