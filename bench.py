@@ -32,10 +32,13 @@ sys.path.insert(0, ROOT)
 METRIC = ("MoE-layer tokens/sec at Hy3 shape; achieved HBM GB/s (decode) and TFLOP/s (prefill) vs peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of the routed GEMM-1 kernel per launch at the decode workload,
-# from the ncu capture summarised in profiles/ (dram__bytes_read.sum +
-# dram__bytes_write.sum), valid only for the gemm.cu it was taken on.
-GEMM1_TRAFFIC = {"gemm_cu_sha": None, "bytes": None}
+# DRAM traffic of the routed GEMM-1 kernel (weights-as-M tiling) from the ncu
+# capture summarised in profiles/gemm_gate_up_decode_e48.md:
+# dram__bytes_read.sum + dram__bytes_write.sum = 1.2122 GB + 4.12 MB for 48
+# touched experts, i.e. 25.34 MB per touched expert. It is scaled to a launch
+# by the touched-expert count (each expert's weights stream once), and only
+# reported while gemm.cu is the source the capture was taken on.
+GEMM1_TRAFFIC = {"gemm_cu_sha": "e729a2c2a24a14b9", "bytes_per_touched_expert": (1.2122e9 + 4.12e6) / 48}
 
 
 def parse():
@@ -47,6 +50,8 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the routed expert count (smaller device footprint for profiler captures)")
     return ap.parse_args()
 
 
@@ -193,7 +198,8 @@ def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None
                          tokens=np.array([0], np.int32))
     t1 = time.perf_counter() - t0
     n = max(1, int(budget_s / max(t1, 1e-6)))
-    n = min(n, shape.T if max_tokens is None else max_tokens)
+    if max_tokens is not None:
+        n = min(n, max_tokens)
     toks = (np.arange(n) % shape.T).astype(np.int32)
     t0 = time.perf_counter()
     oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
@@ -219,6 +225,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     shape = synth.WORKLOADS[args.workload]
+    if args.experts:
+        shape = shape.with_(E=args.experts)
     moe.load()  # fails loudly when the library is not built
 
     x, logits = synth.make_activations(shape, device=dev, seed=rank)
@@ -286,8 +294,9 @@ def run_ours(args):
         achieved = work["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
         peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         unit = "TFLOP/s"
-    traffic = GEMM1_TRAFFIC["bytes"] if (GEMM1_TRAFFIC["gemm_cu_sha"] == gemm_cu_sha()
-                                         and args.workload == "decode") else None
+    traffic = None
+    if GEMM1_TRAFFIC["gemm_cu_sha"] == gemm_cu_sha() and args.workload == "decode":
+        traffic = int(GEMM1_TRAFFIC["bytes_per_touched_expert"] * work["touched"])
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1
@@ -306,7 +315,8 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
         "config": {
-            "workload": f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer",
+            "workload": (f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer")
+                        + (f" with E={shape.E}" if args.experts else ""),
             "T": shape.T, "H": shape.H, "E": shape.E, "K": shape.K, "I": shape.I, "I_shared": shape.I_shared,
             "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
             "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
@@ -336,8 +346,8 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         rate, n, dt, thr = cpu_oracle_rate(shape, x, logits, w, budget_s=12.0)
         result["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
-                                  "sample": f"{n} tokens of the {args.workload} workload through the fp64 oracle "
-                                            f"({dt:.1f} s)"}
+                                  "sample": f"{n} tokens of the {args.workload} workload (its {shape.T} tokens "
+                                            f"cycled) through the fp64 oracle ({dt:.1f} s)"}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
