@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed"])
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--experts", type=int, default=None,
@@ -167,12 +167,13 @@ def algorithmic_work(shape, counts):
     """Bytes the layer must move and FLOPs it must do, from the expert counts."""
     H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
     touched = int((counts > 0).sum())
-    w_expert = 3 * H * I * 2
-    w_shared = 3 * H * Is * 2
-    layer_bytes = touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2
+    wb = 1 + 1 / 32 if shape.dtype == "mxfp8" else 2  # bytes per weight element (E4M3 + E8M0/32, or bf16)
+    w_expert = 3 * H * I * wb
+    w_shared = 3 * H * Is * wb
+    layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2)
     flops = 6 * H * I * T * K + 6 * H * Is * T
     TK = T * K
-    gemm1_bytes = touched * 2 * I * H * 2 + TK * H * 2 + TK * I * 2
+    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * 2 + TK * I * 2)
     return dict(touched=touched, layer_bytes=layer_bytes, flops=flops, gemm1_bytes=gemm1_bytes,
                 gemm1_flops=4 * H * I * TK)
 
@@ -285,7 +286,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     g1_ms = stage_ms["gemm_gate_up"]
-    bound = "hbm" if args.workload in ("decode", "tiny") else "tensor"
+    bound = "hbm" if args.workload in ("decode", "tiny", "mxfp8") else "tensor"
     if bound == "hbm":
         achieved = work["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
@@ -312,7 +313,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "mxfp8 (E4M3 weights + E8M0/32; bf16 tensor-core inputs, fp32 accumulate)"
+                 if shape.dtype == "mxfp8" else "bf16",
         "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
         "config": {
             "workload": (f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer")

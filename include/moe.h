@@ -160,8 +160,9 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
                                  void* x_perm, uint8_t* x_perm_scale, void* ws, size_t ws_bytes,
                                  moe_stream_t stream);
 
-/* Scratch bytes moe_grouped_swiglu_gemm needs: the [rows, I] intermediate. */
-MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int I, moe_dtype_t dtype,
+/* Scratch bytes moe_grouped_swiglu_gemm needs: the [rows, I] bf16
+ * intermediate, plus (MXFP8) the [rows, H] bf16 expansion of `a`. */
+MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int H, int I, moe_dtype_t dtype,
                                                      size_t* bytes);
 
 /* Step 3, the grouped expert GEMM with SwiGLU (the grouped GMM of [Hy3]
@@ -169,7 +170,12 @@ MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int I, moe_dtype_
  *   h = silu(a W_gate[g]^T) * (a W_up[g]^T)   (fp32 accumulate, h stored bf16
  *                                              or, in MXFP8 mode, re-quantised)
  *   y = h W_down[g]^T                          (fp32 accumulate, stored fp32)
- * a (device): [rows, H] bf16 (MXFP8: E4M3 + a_scale [rows, H/32]).
+ * a (device): [rows, H] bf16 (MXFP8: E4M3 codes + a_scale [rows, H/32] E8M0).
+ * MXFP8: w_* are E4M3 codes and s_gate, s_up: [num_groups*I, H/32],
+ *   s_down: [num_groups*H, I/32] their E8M0 scales; h is rounded to MXFP8
+ *   (blocks of 32 along I) before GEMM-2, as the W8A8 path quantises every
+ *   Linear input ([Hy3] section 8.2). The weights stream from HBM as E4M3 and
+ *   are expanded exactly to bf16 in shared memory for the tensor cores.
  * offsets (device): [num_groups + 1] int32, non-decreasing, offsets[0] = 0,
  *   offsets[num_groups] <= rows; NULL means one group of all rows (a dense
  *   SwiGLU MLP, used for the shared expert).
@@ -209,7 +215,9 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
  * `main` at entry is waited on by `side`, which runs the shared expert and
  * records a second event that `main` waits on before the combine.
  * side == NULL runs the shared expert on `main` before the routed path.
- * x (device): [T, H] bf16 (MXFP8 mode: quantised inside, per call).
+ * x (device): [T, H] bf16 (MXFP8 mode: quantised inside, per call, with the
+ * rule of moe_quantize_mxfp8; weights must then be E4M3 + scales, for
+ * example from moe_quantize_mxfp8 on the bf16 weights, and H % 128 == 0).
  * logits (device): [T, E] fp32. out (device): [T, H] bf16.
  * ws (device): at least moe_workspace_size bytes. */
 MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,

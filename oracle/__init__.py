@@ -56,6 +56,7 @@ def _load():
             lib.oracle_swiglu_mlp.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_layer_forward.argtypes = [i, i, i, i, i, i, d, i] + [P] * 8 + [i, P, P, P, P]
             lib.oracle_layer_forward_mx.argtypes = [i, i, i, i, i, i, d, i] + [P] * 14 + [i, P, P]
+            lib.oracle_swiglu_mlp_mx.argtypes = [i, i, i] + [P] * 9
             lib.oracle_mx_quantize_bf16.argtypes = [i, i, P, P, P]
             lib.oracle_mx_quantize_f64.argtypes = [i, i, P, P, P]
             lib.oracle_mx_dequantize.argtypes = [i, i, P, P, P]
@@ -223,3 +224,22 @@ def layer_forward_mx(x, logits, mx_w, *, K: int, scaling: float, route_norm: boo
     _check(_load().oracle_layer_forward_mx(T, H, E, K, I, Is, float(scaling), int(route_norm), _ptr(x), _ptr(logits),
                                            *[_ptr(a) for a in arrs], n, _ptr(tokens), _ptr(out)), "layer_forward_mx")
     return out
+
+
+def swiglu_mlp_mx(xq: np.ndarray, xs: np.ndarray, w_gate, w_up, w_down) -> np.ndarray:
+    """Dense SwiGLU MLP on MX-quantised rows with MX weights ([Hy3] section 8.2).
+
+    xq/xs: codes [R, H] and scales [R, H/32]; w_*: (codes, scales) pairs with
+    w_gate/w_up codes [I, H] and w_down codes [H, I]. Returns float64 [R, H].
+    """
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.uint8)
+    R, H = xq.shape
+    I = w_gate[0].shape[0]
+    arrs = []
+    for q, sc in (w_gate, w_up, w_down):
+        arrs += [np.ascontiguousarray(q, dtype=np.uint8), np.ascontiguousarray(sc, dtype=np.uint8)]
+    y = np.empty((R, H), np.float64)
+    _check(_load().oracle_swiglu_mlp_mx(R, H, I, _ptr(xq), _ptr(xs), *[_ptr(a) for a in arrs], _ptr(y)),
+           "swiglu_mlp_mx")
+    return y

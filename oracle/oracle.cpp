@@ -411,6 +411,23 @@ static void swiglu_row_mx(int H, int I, const double* x, const uint8_t* qg,
   }
 }
 
+// Dense SwiGLU MLP over rows whose activations are already MX-quantised
+// (xq codes [R, H], xs scales [R, H/32]) with MX weights: dequantise x, then
+// the same row function as the MXFP8 layer (h re-quantised per 32 along I).
+// [Hy3] section 8.2: routed and shared Linears in W8A8 MXFP8.
+int oracle_swiglu_mlp_mx(int R, int H, int I, const uint8_t* xq, const uint8_t* xs,
+                         const uint8_t* qg, const uint8_t* sg, const uint8_t* qu,
+                         const uint8_t* su, const uint8_t* qd, const uint8_t* sd, double* y) {
+  if (R < 0 || H <= 0 || H % 32 || I <= 0 || I % 32) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < R; ++r) {
+    std::vector<double> xd(H);
+    oracle_mx_dequantize(1, H, xq + (size_t)r * H, xs + (size_t)r * (H / 32), xd.data());
+    swiglu_row_mx(H, I, xd.data(), qg, sg, qu, su, qd, sd, y + (size_t)r * H);
+  }
+  return 0;
+}
+
 // The whole layer in MXFP8 mode for a subset of tokens. x is given as bf16 and
 // is MX-quantised here (dynamic activation quantisation); weights are given as
 // MX codes/scales (produced by oracle_mx_quantize_bf16 from the bf16 weights).

@@ -75,7 +75,7 @@ def load(build_if_missing: bool = False):
         "moe_route": [P, P, P, P, P, P],
         "moe_permute_workspace_size": [P, PS],
         "moe_permute": [P, P, P, P, P, P, P, P, P, P, P, P, S, P],
-        "moe_grouped_gemm_workspace_size": [I, I, I, PS],
+        "moe_grouped_gemm_workspace_size": [I, I, I, I, PS],
         "moe_grouped_swiglu_gemm": [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, S, P],
         "moe_combine": [P, P, P, P, P, P, P, P],
         "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
@@ -134,9 +134,9 @@ def permute_workspace_size(cfg: Config) -> int:
     return n.value
 
 
-def grouped_gemm_workspace_size(rows: int, I: int, dtype: int = MOE_BF16) -> int:
+def grouped_gemm_workspace_size(rows: int, H: int, I: int, dtype: int = MOE_BF16) -> int:
     n = ctypes.c_size_t(0)
-    _check(load().moe_grouped_gemm_workspace_size(int(rows), int(I), int(dtype), ctypes.byref(n)),
+    _check(load().moe_grouped_gemm_workspace_size(int(rows), int(H), int(I), int(dtype), ctypes.byref(n)),
            "moe_grouped_gemm_workspace_size")
     return n.value
 
@@ -228,6 +228,24 @@ def quantize_mxfp8(h: Handle, x, q, scale, stream=None):
            "moe_quantize_mxfp8")
 
 
+def quantize_mx(h: Handle, t, stream=None):
+    """MXFP8 codes (uint8, same shape) and E8M0 scales (uint8, last dim / 32) of a bf16 tensor."""
+    q = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+    sc = torch.empty(t.shape[:-1] + (t.shape[-1] // 32,), dtype=torch.uint8, device=t.device)
+    quantize_mxfp8(h, t, q, sc, stream=stream)
+    return q, sc
+
+
+def quantize_weights_mx(h: Handle, w: dict, stream=None) -> dict:
+    """MX form of a bf16 weight dict: w_* -> E4M3 codes, s_* / ss_* -> scales."""
+    out = {}
+    for k, v in w.items():
+        q, sc = quantize_mx(h, v, stream=stream)
+        out[k] = q
+        out[("ss_" + k[3:]) if k.startswith("ws_") else ("s_" + k[2:])] = sc
+    return out
+
+
 def make_weights(w: dict) -> Weights:
     ws = Weights()
     for k in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down", "s_gate", "s_up", "s_down",
@@ -262,6 +280,9 @@ class MoELayer:
                                shape.route_norm, MOE_MXFP8_E4M3 if shape.dtype == "mxfp8" else MOE_BF16)
         self.handle = Handle(self.device.index)
         self.ws = torch.empty(workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
+        if shape.dtype == "mxfp8" and weights["w_gate"].dtype != torch.uint8:
+            weights = quantize_weights_mx(self.handle, weights)
+            torch.cuda.synchronize(self.device)
         self.weights_t = weights
         self.weights = make_weights(weights)
         self.side = torch.cuda.Stream(device=self.device) if side_stream else None

@@ -58,6 +58,7 @@ moe_status_t check_cfg(const moe_config_t* c) {
   const long long wide = c->H > c->I ? c->H : c->I;
   if ((long long)c->T * c->K * wide >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (c->dtype == MOE_MXFP8_E4M3 && c->H % 128) return MOE_ERR_INVALID_ARG;  // scale rows in 4-byte units
   if (!(c->scaling == c->scaling)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -65,7 +66,7 @@ moe_status_t check_cfg(const moe_config_t* c) {
 // Workspace layout of moe_layer_forward, every piece 256-byte aligned.
 struct Layout {
   size_t topk_idx, topk_w, counts, offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
-      y_perm, s, h_shared, x_stage, logits_stage, out_stage, total;
+      y_perm, s, h_shared, x_stage, logits_stage, out_stage, x_mx, total;
 };
 
 Layout layout_of(const moe_config_t* c) {
@@ -92,6 +93,7 @@ Layout layout_of(const moe_config_t* c) {
   L.x_stage = take(T * H * 2);
   L.logits_stage = take(T * E * 4);
   L.out_stage = take(T * H * 2);
+  L.x_mx = take(c->dtype == MOE_MXFP8_E4M3 ? T * H * 2 : 0);  // MX-rounded x as bf16
   L.total = off;
   return L;
 }
@@ -111,8 +113,13 @@ moe_status_t check_handle(moe_handle_t h) {
 
 GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int rows, int H, int I,
                           const void* a, const void* wg, const void* wu, const void* wd, void* hbuf,
-                          float* y) {
+                          float* y, const uint8_t* sg = nullptr, const uint8_t* su = nullptr,
+                          const uint8_t* sd = nullptr) {
   GroupedGemmArgs g;
+  g.mx = sg != nullptr;
+  g.s_gate = sg;
+  g.s_up = su;
+  g.s_down = sd;
   g.G = G;
   g.offsets = offsets;
   g.rows = rows;
@@ -264,7 +271,6 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (mx && (!aligned16(x_scale) || !aligned16(x_perm_scale))) return MOE_ERR_INVALID_ARG;
-  if (mx && cfg->H % 512) return MOE_ERR_UNSUPPORTED;  // scale rows gathered as 16-byte vectors
   if (ws_bytes < permute_scratch_bytes(cfg->T * cfg->K, cfg->E)) return MOE_ERR_WORKSPACE;
   if ((st = check_handle(h)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -280,11 +286,13 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
   return cuda_status(e);
 }
 
-MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int I, moe_dtype_t dtype,
+MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int H, int I, moe_dtype_t dtype,
                                                      size_t* bytes) {
-  if (!bytes || rows < 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (!bytes || rows < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  *bytes = align_up((size_t)rows * I * 2 + 1, 256);
+  size_t n = align_up((size_t)rows * I * 2 + 1, 256);                         // h
+  if (dtype == MOE_MXFP8_E4M3) n += align_up((size_t)rows * H * 2 + 1, 256);  // dequantised a
+  *bytes = n;
   return MOE_OK;
 }
 
@@ -295,28 +303,34 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
                                              const void* w_down, const uint8_t* s_gate,
                                              const uint8_t* s_up, const uint8_t* s_down, float* y,
                                              void* ws, size_t ws_bytes, moe_stream_t stream) {
-  (void)a_scale;
-  (void)s_gate;
-  (void)s_up;
-  (void)s_down;
   if (num_groups <= 0 || num_groups > 1024 || rows < 0 || H <= 0 || I <= 0 || H % 64 || I % 64)
     return MOE_ERR_INVALID_ARG;
   if (offsets == nullptr && num_groups != 1) return MOE_ERR_INVALID_ARG;
   if ((long long)rows * (H > I ? H : I) >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
+  const bool mx = dtype == MOE_MXFP8_E4M3;
   if (!a || !w_gate || !w_up || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (mx && (!a_scale || !s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {a, offsets, w_gate, w_up, w_down, y, ws};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8_E4M3) return MOE_ERR_UNSUPPORTED;
   size_t need = 0;
-  moe_grouped_gemm_workspace_size(rows, I, dtype, &need);
+  moe_grouped_gemm_workspace_size(rows, H, I, dtype, &need);
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, a, w_gate, w_up, w_down, ws, y);
-  cudaError_t e = launch_gemm_gate_up(g, s);
+  void* hbuf = ws;
+  const void* act = a;
+  cudaError_t e = cudaSuccess;
+  if (mx) {  // activations arrive as E4M3 + E8M0: expand them once to exact bf16
+    void* adq = static_cast<uint8_t*>(ws) + align_up((size_t)rows * I * 2 + 1, 256);
+    e = launch_mx_dequantize(static_cast<const uint8_t*>(a), a_scale, rows, H, adq, s);
+    act = adq;
+  }
+  GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, act, w_gate, w_up, w_down, hbuf,
+                                y, mx ? s_gate : nullptr, mx ? s_up : nullptr, mx ? s_down : nullptr);
+  if (e == cudaSuccess) e = launch_gemm_gate_up(g, s);
   if (e == cudaSuccess) e = launch_gemm_down(g, s);
   return cuda_status(e);
 }
@@ -342,7 +356,8 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
   if (!aligned16(in_bf16) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
-  return cuda_status(launch_mx_quantize(in_bf16, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
@@ -356,10 +371,12 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
   if (cfg->T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
   if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
+  const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
+  if (mx && (!w->s_gate || !w->s_up || !w->s_down)) return MOE_ERR_INVALID_ARG;
+  if (mx && has_shared && (!w->ss_gate || !w->ss_up || !w->ss_down)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, logits, out, ws, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
-  if (cfg->dtype == MOE_MXFP8_E4M3) return MOE_ERR_UNSUPPORTED;
   const Layout L = layout_of(cfg);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if ((st = check_handle(h)) != MOE_OK) return st;
@@ -396,6 +413,11 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
 
   cudaError_t e = cudaSuccess;
   mark(0, sm);
+  if (mx) {  // dynamic MXFP8 quantisation of x; the GEMMs take the exact bf16 expansion
+    void* xq = at<void>(ws, L.x_mx);
+    e = launch_mx_quantize(x, T, H, nullptr, nullptr, xq, sm);
+    x = xq;
+  }
   cudaStream_t s_sh = ss ? ss : sm;
   if (has_shared) {
     if (ss) {
@@ -404,7 +426,8 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
     }
     mark(6, s_sh);
     GroupedGemmArgs g = gemm_args(h, 1, nullptr, T, H, Is, x, w->ws_gate, w->ws_up, w->ws_down,
-                                  h_shared, s_out);
+                                  h_shared, s_out, mx ? w->ss_gate : nullptr,
+                                  mx ? w->ss_up : nullptr, mx ? w->ss_down : nullptr);
     if (e == cudaSuccess) e = launch_gemm_gate_up(g, s_sh);
     if (e == cudaSuccess) e = launch_gemm_down(g, s_sh);
     mark(7, s_sh);
@@ -420,7 +443,8 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
     e = launch_gather_rows(x, T, H * 2, perm_src, K, TK, x_perm, h->status, sm);
   mark(2, sm);
   GroupedGemmArgs g = gemm_args(h, E, offsets, TK, H, I, x_perm, w->w_gate, w->w_up, w->w_down,
-                                hbuf, y_perm);
+                                hbuf, y_perm, mx ? w->s_gate : nullptr, mx ? w->s_up : nullptr,
+                                mx ? w->s_down : nullptr);
   if (e == cudaSuccess) e = launch_gemm_gate_up(g, sm);
   mark(3, sm);
   if (e == cudaSuccess) e = launch_gemm_down(g, sm);

@@ -48,6 +48,10 @@ struct GroupedGemmArgs {
   void* h;                 // [rows, I] bf16 (intermediate)
   float* y;                // [rows, H] fp32
   int mode;                // GemmMode
+  int mx;                  // 1: weights are E4M3 + E8M0/32 (h MX-rounded too)
+  const uint8_t* s_gate;   // MX scales [G*I, H/32], [G*I, H/32], [G*H, I/32]
+  const uint8_t* s_up;
+  const uint8_t* s_down;
   int num_sms;
   int* status;
   uint64_t wait_limit_ns;
@@ -62,8 +66,12 @@ cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32
                            cudaStream_t s);
 
 // ---- MX quantiser (mxquant.cu)
+// q / scale / deq may each be null; deq receives the dequantised values as bf16.
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, cudaStream_t s);
+                               uint8_t* scale, void* deq, cudaStream_t s);
+// out[r, c] = bf16(e4m3(q[r, c]) * 2^(scale[r, c/32] - 127)).
+cudaError_t launch_mx_dequantize(const uint8_t* q, const uint8_t* scale, int64_t rows, int cols,
+                                 void* out_bf16, cudaStream_t s);
 
 // ---- self-test of the bounded wait (gemm.cu)
 cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t s);

@@ -7,24 +7,23 @@
 //   scale code = clamp(shared_exp, -127, 127) + 127;  amax == 0 -> code 0
 //   element    = RNE(v / 2^shared_exp) to E4M3, saturating at +-448
 // One thread per block of 32: 64 bytes in (four 16-byte loads), 32 code
-// bytes out (two 16-byte stores) and one scale byte.
+// bytes out (two 16-byte stores) and one scale byte; optionally the
+// dequantised block as bf16 (exact: an E4M3 value times a power of two).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "mx.cuh"
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float pow2f(int e) {  // exact 2^e for -127 <= e <= 127
-  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
 __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__ in,
                                                        long long nblocks,
                                                        uint4* __restrict__ q,
-                                                       uint8_t* __restrict__ scale) {
+                                                       uint8_t* __restrict__ scale,
+                                                       uint4* __restrict__ deq) {
   const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nblocks) return;
   uint4 raw[4];
@@ -39,40 +38,71 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
     amax = fmaxf(amax, fabsf(f[j]));
   }
   uint32_t words[8];
+  int code = 0;
   if (amax == 0.0f) {
-    scale[b] = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) words[j] = 0u;
   } else {
-    const int e_amax = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2 amax)
-    int sexp = e_amax - 8;  // fp32-subnormal amax lands below -127 and clamps
-    sexp = sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
-    scale[b] = (uint8_t)(sexp + 127);
-    const float inv = pow2f(-sexp);
+    const int sexp = mx_shared_exp(amax);  // an fp32-subnormal amax clamps to -127
+    code = sexp + 127;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t w = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(f[4 * j + k] * inv, __NV_SATFINITE, __NV_E4M3);
-        w |= (uint32_t)c << (8 * k);
-      }
+      for (int k = 0; k < 4; ++k) w |= mx_encode(f[4 * j + k], sexp) << (8 * k);
       words[j] = w;
     }
   }
-  q[b * 2] = make_uint4(words[0], words[1], words[2], words[3]);
-  q[b * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
+  if (scale) scale[b] = (uint8_t)code;
+  if (q) {
+    q[b * 2] = make_uint4(words[0], words[1], words[2], words[3]);
+    q[b * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
+  }
+  if (deq) {
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) e4m3x4_to_bf16(words[j], code, o[2 * j], o[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) deq[b * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) mx_dequant_kernel(const uint4* __restrict__ q,
+                                                         const uint8_t* __restrict__ scale,
+                                                         long long nblocks,
+                                                         uint4* __restrict__ out) {
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  const uint4 q0 = __ldg(q + b * 2), q1 = __ldg(q + b * 2 + 1);
+  const int sc = scale[b];
+  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  uint32_t o[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) e4m3x4_to_bf16(words[j], sc, o[2 * j], o[2 * j + 1]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) out[b * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
 }  // namespace
 
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, cudaStream_t s) {
+                               uint8_t* scale, void* deq, cudaStream_t s) {
   const long long nblocks = (long long)rows * (cols / 32);
   if (nblocks == 0) return cudaSuccess;
   const long long grid = (nblocks + 255) / 256;
   mx_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
-                                                 reinterpret_cast<uint4*>(q), scale);
+                                                 reinterpret_cast<uint4*>(q), scale,
+                                                 static_cast<uint4*>(deq));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_dequantize(const uint8_t* q, const uint8_t* scale, int64_t rows, int cols,
+                                 void* out_bf16, cudaStream_t s) {
+  const long long nblocks = (long long)rows * (cols / 32);
+  if (nblocks == 0) return cudaSuccess;
+  const long long grid = (nblocks + 255) / 256;
+  mx_dequant_kernel<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(q), scale, nblocks,
+                                                   static_cast<uint4*>(out_bf16));
   return cudaGetLastError();
 }
 

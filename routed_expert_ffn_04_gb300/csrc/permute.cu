@@ -138,11 +138,13 @@ __global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
   }
 }
 
-// One warp per destination row; each lane copies 16-byte vectors, four in flight.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
-                                                          int src_rows, int vecs,
+// One warp per destination row; each lane copies vectors (16 bytes, or 4
+// for short rows such as MX scale rows), four in flight.
+template <typename V>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ src, int src_rows,
+                                                          int vecs,
                                                           const int32_t* __restrict__ perm_src,
-                                                          int K, int TK, uint4* __restrict__ dst,
+                                                          int K, int TK, V* __restrict__ dst,
                                                           int* status) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -150,17 +152,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (int r = gw; r < TK; r += nw) {
     const int f = __ldg(perm_src + r);
     const int t = ((unsigned)f < (unsigned)TK) ? f / K : -1;
-    uint4* d = dst + (size_t)r * vecs;
+    V* d = dst + (size_t)r * vecs;
     if (t < 0 || t >= src_rows) {
       if (lane == 0) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
-      for (int v = lane; v < vecs; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < vecs; v += 32) d[v] = V{};
       continue;
     }
-    const uint4* s = src + (size_t)t * vecs;
+    const V* s = src + (size_t)t * vecs;
     int v = lane;
     for (; v + 96 < vecs; v += 128) {
-      const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64),
-                  a3 = __ldg(s + v + 96);
+      const V a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64), a3 = __ldg(s + v + 96);
       d[v] = a0;
       d[v + 32] = a1;
       d[v + 64] = a2;
@@ -201,12 +202,17 @@ cudaError_t launch_gather_rows(const void* src, int src_rows, int row_bytes,
                                const int32_t* perm_src, int K, int TK, void* dst, int* status,
                                cudaStream_t s) {
   if (TK == 0) return cudaSuccess;
-  const int vecs = row_bytes / 16;
-  long long warps_needed = TK;
-  int blocks = (int)((warps_needed + 7) / 8);
+  int blocks = (TK + 7) / 8;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), src_rows, vecs,
-                                            perm_src, K, TK, static_cast<uint4*>(dst), status);
+  if (row_bytes % 16 == 0) {
+    gather_rows_kernel<uint4><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), src_rows,
+                                                     row_bytes / 16, perm_src, K, TK,
+                                                     static_cast<uint4*>(dst), status);
+  } else {
+    gather_rows_kernel<uint32_t><<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(src), src_rows,
+                                                        row_bytes / 4, perm_src, K, TK,
+                                                        static_cast<uint32_t*>(dst), status);
+  }
   return cudaGetLastError();
 }
 

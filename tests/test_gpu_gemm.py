@@ -35,7 +35,7 @@ def _run(handle, a, offsets, wg, wu, wd, H, I, mode, G):
     rows = a.shape[0]
     handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
     y = torch.full((rows, H), float("nan"), dtype=torch.float32, device="cuda")
-    ws = torch.empty(moe.grouped_gemm_workspace_size(rows, I), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I), dtype=torch.uint8, device="cuda")
     off = None if offsets is None else torch.tensor(offsets, dtype=torch.int32, device="cuda")
     moe.grouped_swiglu_gemm(handle, a.cuda(), off, wg.cuda(), wu.cuda(), wd.cuda(), y, ws, num_groups=G, H=H, I=I)
     torch.cuda.synchronize()

@@ -88,7 +88,7 @@ def test_scaling_zero_gives_shared_expert_exactly(handle):
     out = run_layer(handle, shape, x, logits, w, scaling=0.0)
     # The shared expert alone, through the grouped GEMM entry point (one group).
     y = torch.empty((shape.T, shape.H), dtype=torch.float32, device="cuda")
-    ws = torch.empty(moe.grouped_gemm_workspace_size(shape.T, shape.I_shared), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(moe.grouped_gemm_workspace_size(shape.T, shape.H, shape.I_shared), dtype=torch.uint8, device="cuda")
     moe.grouped_swiglu_gemm(handle, x, None, w["ws_gate"], w["ws_up"], w["ws_down"], y, ws, num_groups=1,
                             H=shape.H, I=shape.I_shared)
     torch.cuda.synchronize()

@@ -1,0 +1,171 @@
+"""GPU parity of the MXFP8 path (E4M3 elements, E8M0 scale per 32 along K)
+against the oracle's MX statement.
+
+The quantiser and the MX permutation are integer/byte work and are compared
+bit-exactly. The MX GEMM and layer are compared with the oracle's MX layer,
+which quantises the bf16 weights with its own quantiser and computes in fp64.
+The bar for MXFP8 outputs is relative L2 <= 3e-2. Because both sides use the
+same quantised operands, the tests also check max-abs <= 2e-2, a tighter
+diagnostic that a mis-indexed block scale would break.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import routed_expert_ffn_04_gb300 as moe
+import synth
+from gpu_common import cfg_of, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+REL_L2_MX = 3e-2
+MAX_ABS_MX = 2e-2
+
+
+@pytest.fixture(scope="module")
+def handle():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    moe.load(build_if_missing=True)
+    return moe.Handle(0)
+
+
+def _check(got, ref, what):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert np.all(np.isfinite(got)), what
+    assert rel <= REL_L2_MX and err.max() <= MAX_ABS_MX, f"{what}: rel_l2={rel:.3e} max_abs={err.max():.3e}"
+    return rel, err.max()
+
+
+def test_quantiser_bit_exact(handle):
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(257, 512, generator=g) * torch.exp(torch.randn(257, 1, generator=g) * 3)
+    x[0, :32] = 0.0                                # zero block -> scale 0, codes 0
+    x[1, :32] = -0.0
+    x[2, 32:64] = 1e-30                            # tiny values (fp32/bf16 subnormal side)
+    x[3, :32] = torch.linspace(-3, 3, 32)
+    x[3, 5] = 1000.0                               # outlier sets the block scale
+    x[4, 64:96] = 2.0 ** 7                         # amax on a binade edge
+    x[5, 96:128] = -448.0 * 2.0 ** -3
+    xb = x.to(torch.bfloat16)
+    q, s = moe.quantize_mx(handle, xb.cuda())
+    torch.cuda.synchronize()
+    rq, rs = oracle.mx_quantize(xb)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_weight_quantisation_matches_oracle(handle):
+    shape = synth.WORKLOADS["tiny"]
+    w = synth.make_weights(shape, seed=1)
+    mx = moe.quantize_weights_mx(handle, {k: v.cuda() for k, v in w.items()})
+    torch.cuda.synchronize()
+    for k, v in w.items():
+        rq, rs = oracle.mx_quantize(v)
+        sk = ("ss_" + k[3:]) if k.startswith("ws_") else ("s_" + k[2:])
+        assert np.array_equal(mx[k].cpu().numpy(), rq), k
+        assert np.array_equal(mx[sk].cpu().numpy(), rs), k
+
+
+@pytest.mark.parametrize("H", [256, 4096])
+def test_mx_permute_gathers_codes_and_scales(handle, H):
+    shape = synth.MoEShape("mxp", T=75, H=H, E=12, K=3, I=128, I_shared=0, dtype="mxfp8")
+    x, logits = synth.make_activations(shape, device="cuda", seed=2)
+    xq, xs = moe.quantize_mx(handle, x)
+    cfg = cfg_of(shape)
+    cfg.dtype = moe.MOE_MXFP8_E4M3
+    TK = shape.T * shape.K
+    idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device="cuda")
+    tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device="cuda")
+    moe.route(handle, cfg, logits, idx, tw)
+    counts = torch.empty(shape.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(shape.E + 1, dtype=torch.int32, device="cuda")
+    perm_src = torch.empty(TK, dtype=torch.int32, device="cuda")
+    f2p = torch.empty(TK, dtype=torch.int32, device="cuda")
+    xpq = torch.empty((TK, H), dtype=torch.uint8, device="cuda")
+    xps = torch.empty((TK, H // 32), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(moe.permute_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.permute(handle, cfg, xq, idx, counts, offsets, perm_src, f2p, xpq, ws, x_scale=xs, x_perm_scale=xps)
+    torch.cuda.synchronize()
+    rc, ro, rp, rf = oracle.permute(idx.cpu().numpy(), shape.E)
+    assert np.array_equal(perm_src.cpu().numpy(), rp)
+    src = torch.from_numpy(rp // shape.K).long().cuda()
+    assert torch.equal(xpq, xq[src]) and torch.equal(xps, xs[src])
+
+
+def _mx_weights_oracle(w):
+    return {k: oracle.mx_quantize(v.cpu()) for k, v in w.items()}
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("H,I,sizes", [(256, 128, [16, 0, 3, 1]), (512, 320, [0, 1, 37, 130, 300, 0])])
+def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(3)
+    a = torch.randn(rows, H, generator=g).to(torch.bfloat16)
+    wg, wu, wd = ((torch.randn(*sh, generator=g) * 0.02).to(torch.bfloat16) for sh in ((G, I, H), (G, I, H), (G, H, I)))
+    aq, as_ = moe.quantize_mx(handle, a.cuda())
+    mw = moe.quantize_weights_mx(handle, {"w_gate": wg.cuda(), "w_up": wu.cuda(), "w_down": wd.cuda()})
+    handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
+    y = torch.full((rows, H), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I, moe.MOE_MXFP8_E4M3), dtype=torch.uint8, device="cuda")
+    moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), mw["w_gate"], mw["w_up"], mw["w_down"], y, ws,
+                            num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP8_E4M3, a_scale=as_, s_gate=mw["s_gate"],
+                            s_up=mw["s_up"], s_down=mw["s_down"])
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    yh = y.cpu().numpy()
+    xq, xs = oracle.mx_quantize(a)
+    for gi in range(G):
+        r0, r1 = offsets[gi], offsets[gi + 1]
+        if r1 == r0:
+            continue
+        ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], oracle.mx_quantize(wg[gi]), oracle.mx_quantize(wu[gi]),
+                                   oracle.mx_quantize(wd[gi]))
+        _check(yh[r0:r1], ref, f"group {gi} mode {mode}")
+    assert np.all(np.isnan(yh[offsets[-1]:]))
+
+
+def _run_mx_layer(handle, shape, x, logits, w_bf16, mode=0):
+    layer = moe.MoELayer(shape, w_bf16, device=0)
+    layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
+    out = layer(x, logits)
+    torch.cuda.synchronize()
+    assert layer.handle.device_status() == 0
+    return out
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_mx_layer_tiny(handle, mode):
+    shape = synth.WORKLOADS["tiny"].with_(dtype="mxfp8")
+    x, logits = synth.make_activations(shape, seed=0)
+    w = synth.make_weights(shape, seed=0)
+    out = _run_mx_layer(handle, shape, x.cuda(), logits.cuda(), {k: v.cuda() for k, v in w.items()}, mode)
+    ref = oracle.layer_forward_mx(x, logits, _mx_weights_oracle(w), K=shape.K, scaling=shape.scaling)
+    _check(out.float().cpu().numpy(), ref, f"tiny mx mode={mode}")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_mx_layer_ragged_shape(handle, mode):
+    shape = synth.MoEShape("mxr", T=45, H=384, E=13, K=3, I=192, I_shared=128, dtype="mxfp8")
+    x, logits = synth.make_activations(shape, seed=5)
+    w = synth.make_weights(shape, seed=5)
+    out = _run_mx_layer(handle, shape, x.cuda(), logits.cuda(), {k: v.cuda() for k, v in w.items()}, mode)
+    ref = oracle.layer_forward_mx(x, logits, _mx_weights_oracle(w), K=shape.K, scaling=shape.scaling)
+    _check(out.float().cpu().numpy(), ref, f"ragged mx mode={mode}")
+
+
+def test_mx_layer_full_size_sampled(handle):
+    shape = synth.WORKLOADS["mxfp8"]
+    x, logits = synth.make_activations(shape, device="cuda", seed=0)
+    w = synth.make_weights(shape, device="cuda", seed=0)
+    out = _run_mx_layer(handle, shape, x, logits, w)
+    tokens = sample_tokens(shape.T, 16, seed=2)
+    ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _mx_weights_oracle(w), K=shape.K, scaling=shape.scaling,
+                                  tokens=tokens)
+    _check(out.float().cpu().numpy()[tokens], ref, "mxfp8 workload")

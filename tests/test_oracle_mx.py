@@ -159,3 +159,22 @@ def test_mx_layer_close_to_bf16_layer_and_pins_scale_indexing():
     wdq_up = _bf16(deq["w_up"].astype(np.float32))
     q2, s2 = oracle.mx_quantize(wdq_up)
     assert np.array_equal(q2, mxw["w_up"][0]) and np.array_equal(s2, mxw["w_up"][1])
+
+
+def test_mx_mlp_on_quantised_rows_matches_numpy_composition():
+    # Pins oracle.swiglu_mlp_mx: numpy matmuls over dequantised operands, with h
+    # re-quantised by the (separately pinned) quantiser.
+    g = torch.Generator().manual_seed(4)
+    R, H, I = 9, 128, 96
+    x = torch.randn(R, H, generator=g).to(torch.bfloat16)
+    w = {k: (torch.randn(*sh, generator=g) * 0.05).to(torch.bfloat16)
+         for k, sh in (("g", (I, H)), ("u", (I, H)), ("d", (H, I)))}
+    xq, xs = oracle.mx_quantize(x)
+    mw = {k: oracle.mx_quantize(v) for k, v in w.items()}
+    y = oracle.swiglu_mlp_mx(xq, xs, mw["g"], mw["u"], mw["d"])
+    xd = oracle.mx_dequantize(xq, xs)
+    dg, du, dd = (oracle.mx_dequantize(*mw[k]) for k in ("g", "u", "d"))
+    gg = xd @ dg.T
+    h = gg / (1.0 + np.exp(-gg)) * (xd @ du.T)
+    hq = oracle.mx_dequantize(*oracle.mx_quantize(h))
+    np.testing.assert_allclose(y, hq @ dd.T, rtol=1e-9, atol=1e-12)
