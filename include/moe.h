@@ -123,8 +123,12 @@ enum {
 };
 
 /* Create a handle on `device`: records the SM count, resolves the TMA
- * descriptor encoder, allocates the device status word and two events.
- * Returns MOE_ERR_CUDA if the device is unusable. */
+ * descriptor encoder, sets the kernels' shared-memory limits on the device,
+ * allocates the device status word and two events. Returns MOE_ERR_CUDA if
+ * the device is unusable. After this, moe_layer_forward makes no allocation
+ * or device-attribute call, so a call (with stage timing off) can be
+ * captured into a CUDA graph on `main`, the side stream joining through the
+ * handle's two events. */
 MOE_API moe_status_t moe_create(int device, moe_handle_t* out);
 MOE_API moe_status_t moe_destroy(moe_handle_t h);
 MOE_API const char* moe_status_string(moe_status_t s);

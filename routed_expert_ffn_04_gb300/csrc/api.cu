@@ -184,7 +184,8 @@ MOE_API moe_status_t moe_create(int device, moe_handle_t* out) {
   if (!h) return MOE_ERR_CUDA;
   h->device = device;
   h->num_sms = sms;
-  if (cudaMalloc(&h->status, 64) != cudaSuccess || cudaMemset(h->status, 0, 64) != cudaSuccess ||
+  if (gemm_prepare_device() != cudaSuccess || cudaMalloc(&h->status, 64) != cudaSuccess ||
+      cudaMemset(h->status, 0, 64) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_sh, cudaEventDisableTiming) != cudaSuccess) {
     moe_destroy(h);

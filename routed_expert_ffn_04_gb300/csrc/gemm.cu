@@ -728,8 +728,6 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
       !make_map(&m_w1, w1, WQ, Kdim, (uint64_t)G * N, 128))
     return cudaErrorInvalidValue;
   auto kern = grouped_gemm_kernel<SWAP, MODE, BN, WQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
-  if (e != cudaSuccess) return e;
   KParams p;
   p.offsets = a.offsets;
   p.G = G;
@@ -748,6 +746,12 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
   kern<<<grid, Gm::THREADS, Gm::SMEM, s>>>(m_act, m_w0, m_w1, p);
   return cudaGetLastError();
+}
+
+template <bool SWAP, int MODE, int BN, bool WQ>
+cudaError_t set_smem_attribute() {
+  return cudaFuncSetAttribute(grouped_gemm_kernel<SWAP, MODE, BN, WQ>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<SWAP, MODE, BN, WQ>::SMEM);
 }
 
 int pick_mode(const GroupedGemmArgs& a) {
@@ -776,6 +780,17 @@ bool gemm_init_driver() {
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   });
   return g_encode != nullptr;
+}
+
+cudaError_t gemm_prepare_device() {
+  const cudaError_t errs[] = {
+      set_smem_attribute<true, 0, 32, false>(), set_smem_attribute<false, 0, 32, false>(),
+      set_smem_attribute<true, 1, 32, false>(), set_smem_attribute<false, 1, 32, false>(),
+      set_smem_attribute<true, 0, 32, true>(),  set_smem_attribute<false, 0, 32, true>(),
+      set_smem_attribute<true, 1, 32, true>(),  set_smem_attribute<false, 1, 32, true>()};
+  for (cudaError_t e : errs)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {

@@ -57,6 +57,9 @@ struct GroupedGemmArgs {
   uint64_t wait_limit_ns;
 };
 bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailable
+// Opt the GEMM kernels into their dynamic shared memory on the current device
+// (once per device, outside any stream capture).
+cudaError_t gemm_prepare_device();
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
 

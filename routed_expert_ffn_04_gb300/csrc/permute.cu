@@ -7,8 +7,9 @@
 // Counting sort in three kernels, deterministic and without float atomics:
 //   1. hist:    each warp counts expert ids over its chunk of 256 flat
 //               indices (shared-memory counters) -> hist[e][w].
-//   2. scan:    one block turns hist (expert-major) into exclusive bases;
-//               offsets[e] = base[e][0], counts[e] = offsets[e+1]-offsets[e].
+//   2. scan:    one block turns hist (expert-major) into exclusive bases
+//               (expert totals, a scan over experts, then per-expert rows);
+//               offsets[e] = base[e][0], counts[e] = the expert's total.
 //   3. scatter: each warp walks its chunk in flat order, 32 at a time; lanes
 //               with equal ids are grouped with __match_any_sync and ranked
 //               by lane order, so rows of one expert keep ascending f.
@@ -48,61 +49,71 @@ __global__ void __launch_bounds__(kWarps * 32) perm_hist_kernel(const int32_t* _
   for (int e = lane; e < E; e += 32) hist[(size_t)e * NW + w] = h[e];
 }
 
-// Exclusive scan of M = E*NW counts in place (expert-major), by one block.
+// Exclusive scan of the E x NW counts in place (expert-major), by one block
+// of 32 warps: (1) warp w sums the rows of experts w, w+32, ... with
+// coalesced loads; (2) one exclusive scan over the E expert totals gives the
+// expert offsets; (3) each warp scans its experts' rows 32 entries at a time,
+// starting from the expert offset.
 __global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* __restrict__ hist, int E,
                                                                  int NW, int32_t* __restrict__ counts,
                                                                  int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[1024];
   __shared__ int32_t warp_tot[32];
-  __shared__ int32_t grand_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (NW == 0) {  // no (token, slot) pairs: every expert is empty
-    for (int e = tid; e <= E; e += kScanThreads) {
-      offsets[e] = 0;
-      if (e < E) counts[e] = 0;
-    }
-    return;
+  for (int e = warp; e < E; e += 32) {
+    const int32_t* row = hist + (size_t)e * NW;
+    int32_t sum = 0;
+    for (int w = lane; w < NW; w += 32) sum += row[w];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+    if (lane == 0) tot[e] = sum;
   }
-  const long long M = (long long)E * NW;
-  const long long per = (M + kScanThreads - 1) / kScanThreads;
-  const long long b = tid * per;
-  const long long e_ = (b + per < M) ? b + per : M;
-  int32_t local = 0;
-  for (long long i = b; i < e_; ++i) local += hist[i];
-  // Block-wide exclusive scan of `local`.
-  int32_t incl = local;
+  __syncthreads();
+  // Block exclusive scan of tot[0..E) (one entry per thread, E <= 1024).
+  const int32_t v = tid < E ? tot[tid] : 0;
+  int32_t incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (lane >= off) incl += v;
+    const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += u;
   }
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int32_t v = warp_tot[lane];
-    int32_t inc2 = v;
+    const int32_t wv = warp_tot[lane];
+    int32_t winc = wv;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, inc2, off);
-      if (lane >= off) inc2 += u;
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, winc, off);
+      if (lane >= off) winc += u;
     }
-    warp_tot[lane] = inc2 - v;  // exclusive prefix of warp totals
-    if (lane == 31) grand_total = inc2;
+    warp_tot[lane] = winc - wv;
   }
   __syncthreads();
-  int32_t run = warp_tot[warp] + incl - local;
-  for (long long i = b; i < e_; ++i) {
-    const int32_t c = hist[i];
-    hist[i] = run;
-    run += c;
+  const int32_t excl = warp_tot[warp] + incl - v;
+  if (tid < E) {
+    offsets[tid] = excl;
+    counts[tid] = v;
+    if (tid == E - 1) offsets[E] = excl + v;
+    tot[tid] = excl;  // expert start, read back below
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kScanThreads) {
-    const int32_t start = hist[(size_t)e * NW];
-    const int32_t end = (e + 1 < E) ? hist[(size_t)(e + 1) * NW] : grand_total;
-    offsets[e] = start;
-    counts[e] = end - start;
+  for (int e = warp; e < E; e += 32) {
+    int32_t* row = hist + (size_t)e * NW;
+    int32_t carry = tot[e];
+    for (int w0 = 0; w0 < NW; w0 += 32) {
+      const int w = w0 + lane;
+      const int32_t c = w < NW ? row[w] : 0;
+      int32_t inc = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+        if (lane >= off) inc += u;
+      }
+      if (w < NW) row[w] = carry + inc - c;
+      carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
   }
-  if (tid == 0) offsets[E] = grand_total;
 }
 
 __global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
@@ -190,9 +201,14 @@ cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* s
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
+  if (NW == 0) {  // no (token, slot) pairs: every expert is empty
+    cudaError_t err = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    return err;
+  }
   perm_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, E, NW, counts, offsets);
   cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess || NW == 0) return err;
+  if (err != cudaSuccess) return err;
   perm_scatter_kernel<<<blocks, kWarps * 32, smem, s>>>(topk_idx, TK, E, NW, hist, perm_src,
                                                          flat_to_perm);
   return cudaGetLastError();
