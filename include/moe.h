@@ -229,6 +229,25 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
                                        void* out, void* ws, size_t ws_bytes, moe_stream_t main,
                                        moe_stream_t side);
 
+/* Gating + routing ([Hy3] section 8.5: the main stream runs gating, then the
+ * routed path): logits = x w_router^T in fp32 (tensor cores, bf16 inputs),
+ * then the routing of moe_route. With E <= 256 one kernel does both: the
+ * top-k runs in the GEMM epilogue on the fp32 accumulators.
+ * x (device): [T, H] bf16; w_router (device): [E, H] bf16;
+ * logits_out (device, nullable when E <= 256): [T, E] fp32;
+ * topk_idx / topk_w (device): [T, K]. E > 256 needs E % 32 == 0. */
+MOE_API moe_status_t moe_gate_route(moe_handle_t h, const moe_config_t* cfg, const void* x,
+                                    const void* w_router, float* logits_out, int32_t* topk_idx,
+                                    float* topk_w, moe_stream_t stream);
+
+/* moe_layer_forward with the gating projection inside: routes from
+ * x w_router^T (moe_gate_route) instead of given logits. In MXFP8 mode the
+ * router reads the bf16 x. E > 256 needs E % 32 == 0. */
+MOE_API moe_status_t moe_layer_forward_gated(moe_handle_t h, const moe_config_t* cfg,
+                                             const moe_weights_t* w, const void* w_router,
+                                             const void* x, void* out, void* ws, size_t ws_bytes,
+                                             moe_stream_t main, moe_stream_t side);
+
 /* The same layer with HOST activations: copies x_host [T, H] bf16 and
  * logits_host [T, E] fp32 to the device (staging inside ws), runs
  * moe_layer_forward, copies out back to out_host [T, H] bf16 and

@@ -52,6 +52,7 @@ def _load():
             P = ctypes.c_void_p
             i, d = ctypes.c_int, ctypes.c_double
             lib.oracle_route.argtypes = [i, i, i, P, d, i, P, P]
+            lib.oracle_gate.argtypes = [i, i, i, P, P, P]
             lib.oracle_permute.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_swiglu_mlp.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_layer_forward.argtypes = [i, i, i, i, i, i, d, i] + [P] * 8 + [i, P, P, P, P]
@@ -97,6 +98,17 @@ def num_threads() -> int:
 
 def set_num_threads(n: int) -> None:
     _load().oracle_set_num_threads(int(n))
+
+
+def gate(x, w_router) -> np.ndarray:
+    """Router logits x w_router^T in float64 ([Hy3] section 8.5, Gating)."""
+    xb, wb = _bf16_bits(x), _bf16_bits(w_router)
+    T, H = xb.shape
+    E = wb.shape[0]
+    assert wb.shape == (E, H)
+    out = np.empty((T, E), np.float64)
+    _check(_load().oracle_gate(T, H, E, _ptr(xb), _ptr(wb), _ptr(out)), "gate")
+    return out
 
 
 def route(logits: np.ndarray, K: int, scaling: float, route_norm: bool = True):

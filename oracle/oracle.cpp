@@ -74,6 +74,25 @@ void oracle_set_num_threads(int n) {
 }
 
 // ---------------------------------------------------------------------------
+// Gating: the router projection that produces the logits routing ranks.
+// [Hy3] section 8.5: the main stream runs Gating first, then the routed path.
+// logits[t, e] = sum_c x[t, c] * w_router[e, c], in double.
+// x: [T, H] bf16; w_router: [E, H] bf16; logits: [T, E] double out.
+// ---------------------------------------------------------------------------
+int oracle_gate(int T, int H, int E, const uint16_t* x, const uint16_t* w_router, double* logits) {
+  if (T < 0 || H <= 0 || E <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int c = 0; c < H; ++c)
+        acc += bf16_to_double(x[(size_t)t * H + c]) * bf16_to_double(w_router[(size_t)e * H + c]);
+      logits[(size_t)t * E + e] = acc;
+    }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Step 1: sigmoid top-k routing with route_norm and router_scaling_factor.
 // [Hy3] section 一: 192 routed experts, top-8 sigmoid routing; HYV3Config
 // defaults router_scaling_factor=2.826, num_experts_per_tok=8, route_norm=True,

@@ -85,6 +85,8 @@ def load(build_if_missing: bool = False):
         "moe_read_stage_times": [P, ctypes.POINTER(F), ctypes.POINTER(I)],
         "moe_selftest_wait_timeout": [P, P],
         "moe_permute_static_scratch": [P, P, P, P, P, P, P, P, P, P, P, P],
+        "moe_gate_route": [P, P, P, P, P, P, P, P],
+        "moe_layer_forward_gated": [P, P, P, P, P, P, P, S, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -244,6 +246,19 @@ def quantize_weights_mx(h: Handle, w: dict, stream=None) -> dict:
         out[k] = q
         out[("ss_" + k[3:]) if k.startswith("ws_") else ("s_" + k[2:])] = sc
     return out
+
+
+def gate_route(h: Handle, cfg: Config, x, w_router, topk_idx, topk_w, logits_out=None, stream=None):
+    """Gating projection + routing (fused in one kernel when E <= 256)."""
+    _check(load().moe_gate_route(h.ptr, ctypes.byref(cfg), _p(x), _p(w_router), _p(logits_out), _p(topk_idx),
+                                 _p(topk_w), _stream(stream)), "moe_gate_route")
+
+
+def layer_forward_gated(h: Handle, cfg: Config, weights: Weights, w_router, x, out, ws, main=None, side=None):
+    side_p = ctypes.c_void_p(side.cuda_stream) if side is not None else None
+    _check(load().moe_layer_forward_gated(h.ptr, ctypes.byref(cfg), ctypes.byref(weights), _p(w_router), _p(x),
+                                          _p(out), _p(ws), ws.numel() * ws.element_size(), _stream(main), side_p),
+           "moe_layer_forward_gated")
 
 
 def make_weights(w: dict) -> Weights:

@@ -116,6 +116,11 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
                           float* y, const uint8_t* sg = nullptr, const uint8_t* su = nullptr,
                           const uint8_t* sd = nullptr) {
   GroupedGemmArgs g;
+  g.topk_idx = nullptr;
+  g.topk_w = nullptr;
+  g.topk = 0;
+  g.scaling = 1.0f;
+  g.route_norm = 0;
   g.mx = sg != nullptr;
   g.s_gate = sg;
   g.s_up = su;
@@ -147,6 +152,28 @@ cudaError_t timing_events(moe_handle_t h) {
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Gating ([Hy3] section 8.5: the main stream runs gating, then the routed
+// path): logits = x W_router^T and the routing of step 1. E <= 256 runs as
+// one kernel with the top-k in the GEMM epilogue; larger E writes the logits
+// (into `logits`, required then) and runs the routing kernel on them.
+cudaError_t gate_route(moe_handle_t h, const moe_config_t* c, const void* x, const void* w_router,
+                       float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+  GroupedGemmArgs g = gemm_args(h, 1, nullptr, c->T, /*H (N)=*/c->E, /*I (K)=*/c->H, x, nullptr,
+                                nullptr, w_router, const_cast<void*>(x), logits);
+  if (c->E <= 256) {
+    g.topk_idx = topk_idx;
+    g.topk_w = topk_w;
+    g.topk = c->K;
+    g.scaling = c->scaling;
+    g.route_norm = c->route_norm;
+    return launch_gate_route(g, s);
+  }
+  cudaError_t e = launch_gemm_down(g, s);
+  if (e == cudaSuccess)
+    e = launch_route(logits, c->T, c->E, c->K, c->scaling, c->route_norm, topk_idx, topk_w, s);
+  return e;
 }
 
 }  // namespace
@@ -361,15 +388,16 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
       launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
-MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
+static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
                                        const moe_weights_t* w, const void* x, const float* logits,
-                                       void* out, void* ws, size_t ws_bytes, moe_stream_t main,
-                                       moe_stream_t side) {
+                                       const void* w_router, void* out, void* ws, size_t ws_bytes,
+                                       moe_stream_t main, moe_stream_t side) {
   moe_status_t st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (!w || !ws) return MOE_ERR_INVALID_ARG;
   const bool has_shared = cfg->I_shared > 0;
-  if (cfg->T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || (!logits && !w_router) || !out)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
   const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
@@ -414,6 +442,7 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
 
   cudaError_t e = cudaSuccess;
   mark(0, sm);
+  const void* x_gate = x;  // the router reads x as given (bf16)
   if (mx) {  // dynamic MXFP8 quantisation of x; the GEMMs take the exact bf16 expansion
     void* xq = at<void>(ws, L.x_mx);
     e = launch_mx_quantize(x, T, H, nullptr, nullptr, xq, sm);
@@ -434,8 +463,12 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
     mark(7, s_sh);
     if (e == cudaSuccess && ss) e = cudaEventRecord(h->ev_sh, ss);  // shared MLP done
   }
-  if (e == cudaSuccess)
-    e = launch_route(logits, T, E, K, cfg->scaling, cfg->route_norm, topk_idx, topk_w, sm);
+  if (e == cudaSuccess) {
+    if (w_router)
+      e = gate_route(h, cfg, x_gate, w_router, at<float>(ws, L.logits_stage), topk_idx, topk_w, sm);
+    else
+      e = launch_route(logits, T, E, K, cfg->scaling, cfg->route_norm, topk_idx, topk_w, sm);
+  }
   mark(1, sm);
   if (e == cudaSuccess)
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
@@ -456,6 +489,39 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
   mark(5, sm);
   if (ev) h->t_calls += 1;
   return cuda_status(e);
+}
+
+MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
+                                       const moe_weights_t* w, const void* x, const float* logits,
+                                       void* out, void* ws, size_t ws_bytes, moe_stream_t main,
+                                       moe_stream_t side) {
+  if (cfg && cfg->T > 0 && !logits) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(h, cfg, w, x, logits, nullptr, out, ws, ws_bytes, main, side);
+}
+
+MOE_API moe_status_t moe_layer_forward_gated(moe_handle_t h, const moe_config_t* cfg,
+                                             const moe_weights_t* w, const void* w_router,
+                                             const void* x, void* out, void* ws, size_t ws_bytes,
+                                             moe_stream_t main, moe_stream_t side) {
+  if (!w_router || (cfg && cfg->E > 256 && cfg->E % 32)) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(h, cfg, w, x, nullptr, w_router, out, ws, ws_bytes, main, side);
+}
+
+MOE_API moe_status_t moe_gate_route(moe_handle_t h, const moe_config_t* cfg, const void* x,
+                                    const void* w_router, float* logits_out, int32_t* topk_idx,
+                                    float* topk_w, moe_stream_t stream) {
+  moe_status_t st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T > 0 && (!x || !w_router || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (cfg->E > 256 && cfg->T > 0 && !logits_out) return MOE_ERR_INVALID_ARG;
+  if (cfg->E > 256 && cfg->E % 32) return MOE_ERR_INVALID_ARG;  // logits GEMM stores 32-column chunks
+  const void* ptrs[] = {x, w_router, logits_out, topk_idx, topk_w};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_handle(h)) != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  return cuda_status(gate_route(h, cfg, x, w_router, logits_out, topk_idx, topk_w,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API moe_status_t moe_layer_forward_host(moe_handle_t h, const moe_config_t* cfg,

@@ -9,6 +9,9 @@
 //   GEMM-1 (MODE 0):  h[r, i] = silu(sum_c a[r,c] Wg[g,i,c]) * (sum_c a[r,c] Wu[g,i,c])
 //   GEMM-2 (MODE 1):  y[r, m] = sum_i h[r,i] Wd[g,m,i]
 // for every row r of group g (rows offsets[g] .. offsets[g+1]-1).
+//   Gating (MODE 2):  logits[t, e] = sum_c x[t,c] Wr[e,c] for E <= 256, one
+//                     group; the epilogue runs the sigmoid top-k routing on
+//                     the fp32 accumulators (section 8.5: gating, then routing).
 //
 // Kernel structure (persistent, one CTA per SM):
 //   warp 0      TMA producer (one thread): fills a ring of shared-memory
@@ -47,6 +50,7 @@
 #include "internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
+#include "topk_key.cuh"
 
 namespace moe {
 namespace {
@@ -114,6 +118,12 @@ struct KParams {
   const uint8_t* s_w1;
   int sstride;   // Kdim / 32
   int w_rows;    // G * N
+  // Gating (MODE 2): routing outputs [rows, topk]; `out` (nullable) takes the logits.
+  int32_t* topk_idx;
+  float* topk_w;
+  int topk;
+  float scaling;
+  int route_norm;
 };
 
 struct TileInfo {
@@ -248,6 +258,47 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+    } else if (MODE == 2) {
+      // Fused routing of this token: its E logits sit in TMEM columns 0..E-1.
+      // Round k takes the largest key below the previous pick (keys are
+      // unique), so no list of taken experts is kept.
+      const int E = p.N;
+      float* lrow = static_cast<float*>(p.out);
+      if (lrow) lrow += (size_t)(ti.row0 + (rv ? r : 0)) * E;
+      const size_t orow = (size_t)(ti.row0 + (rv ? r : 0)) * p.topk;
+      unsigned long long prev = ~0ull;
+      float sum = 0.0f;
+#pragma unroll 1
+      for (int k = 0; k < p.topk; ++k) {
+        unsigned long long best = 0ull;
+#pragma unroll 1
+        for (int c = 0; c < E; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int e = c + j;
+            const float l = __uint_as_float(v[j]);
+            if (k == 0 && lrow && rv && e < E) lrow[e] = l;
+            const unsigned long long key = e < E ? make_key(l, e) : 0ull;
+            if (key < prev && key > best) best = key;
+          }
+        }
+        prev = best;
+        const float sig = 1.0f / (1.0f + expf(-key_logit(best)));
+        sum += sig;
+        if (rv) {
+          p.topk_idx[orow + k] = key_id(best);
+          p.topk_w[orow + k] = sig;
+        }
+      }
+      if (rv) {
+        for (int k = 0; k < p.topk; ++k) {
+          const float sig = p.topk_w[orow + k];
+          p.topk_w[orow + k] = (p.route_norm ? sig / sum : sig) * p.scaling;
         }
       }
     } else {
@@ -741,6 +792,11 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   p.s_w1 = MODE == 0 ? a.s_up : a.s_down;
   p.sstride = Kdim / 32;
   p.w_rows = G * N;
+  p.topk_idx = a.topk_idx;
+  p.topk_w = a.topk_w;
+  p.topk = a.topk;
+  p.scaling = a.scaling;
+  p.route_norm = a.route_norm;
   const long long n_wt = (N + Gm::W_COLS - 1) / Gm::W_COLS;
   const long long max_tiles = n_wt * ((a.rows + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
@@ -787,7 +843,8 @@ cudaError_t gemm_prepare_device() {
       set_smem_attribute<true, 0, 32, false>(), set_smem_attribute<false, 0, 32, false>(),
       set_smem_attribute<true, 1, 32, false>(), set_smem_attribute<false, 1, 32, false>(),
       set_smem_attribute<true, 0, 32, true>(),  set_smem_attribute<false, 0, 32, true>(),
-      set_smem_attribute<true, 1, 32, true>(),  set_smem_attribute<false, 1, 32, true>()};
+      set_smem_attribute<true, 1, 32, true>(),  set_smem_attribute<false, 1, 32, true>(),
+      set_smem_attribute<false, 2, 32, false>()};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
@@ -799,6 +856,12 @@ cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_mode<1>(a, s);
+}
+
+cudaError_t launch_gate_route(const GroupedGemmArgs& a, cudaStream_t s) {
+  // MODE 2 reads the MODE 1 operand slots: act = a.h (x), K = a.I (hidden),
+  // N = a.H (experts), weights = a.w_down (router).
+  return run_gemm<false, 2, 32, false>(a, s);
 }
 
 cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t s) {

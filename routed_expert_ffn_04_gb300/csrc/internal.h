@@ -47,6 +47,11 @@ struct GroupedGemmArgs {
   const void* w_down;      // [G, H, I] bf16
   void* h;                 // [rows, I] bf16 (intermediate)
   float* y;                // [rows, H] fp32
+  int32_t* topk_idx;       // gating: routing outputs [rows, topk]
+  float* topk_w;
+  int topk;
+  float scaling;
+  int route_norm;
   int mode;                // GemmMode
   int mx;                  // 1: weights are E4M3 + E8M0/32 (h MX-rounded too)
   const uint8_t* s_gate;   // MX scales [G*I, H/32], [G*I, H/32], [G*H, I/32]
@@ -62,6 +67,10 @@ bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailab
 cudaError_t gemm_prepare_device();
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
+// Gating GEMM (one group, E <= 256) with routing in its epilogue: a.h = x
+// [rows, a.I], a.w_down = router weights [a.H = E, a.I], a.y = logits out
+// (nullable), routing into a.topk_idx / a.topk_w.
+cudaError_t launch_gate_route(const GroupedGemmArgs& a, cudaStream_t s);
 
 // ---- combine (combine.cu)
 cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32_t* flat_to_perm,

@@ -11,27 +11,10 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "topk_key.cuh"
 
 namespace moe {
 namespace {
-
-__device__ __forceinline__ unsigned long long make_key(float l, int id) {
-  uint32_t ord;
-  if (l != l) {
-    ord = 0;  // NaN ranks below every number
-  } else {
-    l = l + 0.0f;  // -0 -> +0 so that the two zeros tie
-    const uint32_t u = __float_as_uint(l);
-    ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  }
-  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-
-__device__ __forceinline__ float key_logit(unsigned long long key) {
-  const uint32_t ord = (uint32_t)(key >> 32);
-  const uint32_t u = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
-  return __uint_as_float(u);
-}
 
 template <int VPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E,
@@ -61,7 +44,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
       const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
       best = o > best ? o : best;
     }
-    const int id = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    const int id = key_id(best);
     if ((id & 31) == lane) {
 #pragma unroll
       for (int j = 0; j < VPL; ++j)

@@ -128,3 +128,17 @@ def test_weights_follow_logistic_function_closed_form():
 def test_bad_sizes_rejected():
     with pytest.raises(ValueError):
         oracle.route(np.zeros((2, 3), np.float32), 4, 1.0)
+
+
+def test_gate_matches_numpy_matmul():
+    import torch
+
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(13, 96, generator=g).to(torch.bfloat16)
+    w = (torch.randn(24, 96, generator=g) * 0.1).to(torch.bfloat16)
+    ref = x.double().numpy() @ w.double().numpy().T
+    np.testing.assert_allclose(oracle.gate(x, w), ref, rtol=1e-12, atol=1e-12)
+    # A one-hot router row picks out one input column exactly.
+    w1 = torch.zeros(4, 96, dtype=torch.bfloat16)
+    w1[2, 17] = 1.0
+    assert np.array_equal(oracle.gate(x, w1)[:, 2], x[:, 17].double().numpy())
