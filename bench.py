@@ -194,10 +194,12 @@ def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None
     import oracle as _o
     conv = [_o._bf16_bits(a) for a in args]
     xb = _o._bf16_bits(xh)
+    # Calibrate on a small batch (fixed per-call costs amortised), then size the sample.
+    n_cal = min(shape.T, 16)
     t0 = time.perf_counter()
     oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
-                         tokens=np.array([0], np.int32))
-    t1 = time.perf_counter() - t0
+                         tokens=np.arange(n_cal, dtype=np.int32))
+    t1 = (time.perf_counter() - t0) / n_cal
     n = max(1, int(budget_s / max(t1, 1e-6)))
     if max_tokens is not None:
         n = min(n, max_tokens)
