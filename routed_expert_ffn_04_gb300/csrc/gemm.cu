@@ -75,7 +75,10 @@ struct Geo {
                                    : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
   static constexpr int TABLE_BYTES = (kMaxGroups + 8) * 4;
   static constexpr int BAR_BYTES = 512;
-  static constexpr int EXTRA = 1024 + TABLE_BYTES + BAR_BYTES;
+  // Tokens-as-M epilogue: per-warp 32 x 32 fp32 staging (row stride 33) so
+  // output rows leave as contiguous 128-byte stores.
+  static constexpr int EPI_BYTES = SWAP ? 0 : 4 * 32 * 33 * 4;
+  static constexpr int EXTRA = 1024 + TABLE_BYTES + BAR_BYTES + EPI_BYTES;
   static constexpr int BUDGET = kMaxSmem - EXTRA;
   // bf16 weights: one ring whose stages hold both operands of a K slice.
   static constexpr int STAGE_BYTES = ACT_BYTES + W_BYTES;
@@ -88,7 +91,7 @@ struct Geo {
   static constexpr int RAW_K = 2 * kBK;                              // fp8 K per raw stage (two slices)
   static constexpr int RAW_BYTES = 2 * 128 * RAW_K;                  // two fp8 boxes of 128 x 128
   static constexpr int S_W = WQ ? 3 : 0;
-  static constexpr int S_ACT = WQ ? (SWAP ? 8 : 3) : 0;
+  static constexpr int S_ACT = WQ ? (SWAP ? 8 : 2) : 0;
   static constexpr int S_RAW_FREE = WQ ? (BUDGET - S_W * W_BYTES - S_ACT * ACT_BYTES) / RAW_BYTES : 0;
   static constexpr int S_RAW = S_RAW_FREE > 8 ? 8 : S_RAW_FREE;
   static constexpr int RING_BYTES = WQ ? S_W * W_BYTES + S_ACT * ACT_BYTES + S_RAW * RAW_BYTES
@@ -182,7 +185,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // MX-rounded when MXH) or y (fp32). Executed by one warp for its 32 lanes.
 template <bool SWAP, int MODE, int BN, bool MXH>
 __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& ti, uint32_t tb,
-                                              int q, int lane) {
+                                              int q, int lane, float* stg) {
   if (SWAP) {
     // TMEM lane = weight row (output column), TMEM column = token.
     const int r_first = ti.tt * BN;
@@ -302,19 +305,26 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
         }
       }
     } else {
-      float* yrow = static_cast<float*>(p.out) + (size_t)(ti.row0 + (rv ? r : 0)) * p.N;
+      // fp32 y: each 32 x 32 block goes through the warp's staging tile so
+      // that every store instruction writes 128 contiguous bytes of one row.
+      const int r_first = ti.tt * 128 + q * 32;  // this warp's first row in the group
+      float* y = static_cast<float*>(p.out);
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tb + c, v);
         tmem_ld_wait();
         const int col = ti.wt * 256 + c;
-        if (rv && col < p.N) {
-          float4* dst = reinterpret_cast<float4*>(yrow + col);
+        if (col < p.N) {  // warp-uniform
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
+          __syncwarp();
+#pragma unroll 4
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = r_first + rr;
+            if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+          }
+          __syncwarp();
         }
       }
     }
@@ -360,6 +370,7 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN, WQ>::THREADS, 1)
   uint8_t* w_ring_p = base;
   const uint8_t* raw_ring_p = base + (raw_ring - base_u32);
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + Gm::RING_BYTES);
+  float* epi_stage = reinterpret_cast<float*>(base + Gm::RING_BYTES + Gm::TABLE_BYTES + Gm::BAR_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::RING_BYTES + Gm::TABLE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Gm::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -581,7 +592,7 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN, WQ>::THREADS, 1)
       tc_fence_after();
       const TileInfo ti = decode_tile<Gm::ACT_ROWS>(p, tile_start, tile);
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Gm::ACC_COLS);
-      epilogue_tile<SWAP, MODE, BN, WQ>(p, ti, tb, q, lane);
+      epilogue_tile<SWAP, MODE, BN, WQ>(p, ti, tb, q, lane, epi_stage + q * 32 * 33);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
