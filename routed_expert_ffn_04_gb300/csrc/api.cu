@@ -67,6 +67,9 @@ moe_status_t check_cfg(const moe_config_t* c) {
 struct Layout {
   size_t topk_idx, topk_w, counts, offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
       y_perm, s, h_shared, x_stage, logits_stage, out_stage, x_mx, total;
+  // MXFP8 only: E8M0 scales of x (x_mx holds its E4M3 codes), of the permuted
+  // x, of h and of the shared expert's h.
+  size_t x_mx_s, x_perm_s, h_s, h_shared_s;
 };
 
 Layout layout_of(const moe_config_t* c) {
@@ -85,15 +88,21 @@ Layout layout_of(const moe_config_t* c) {
   L.perm_src = take(TK * 4);
   L.flat_to_perm = take(TK * 4);
   L.perm_scratch = take(permute_scratch_bytes((int)TK, (int)E));
-  L.x_perm = take(TK * H * 2);
-  L.h = take(TK * I * 2);
+  const bool mx = c->dtype == MOE_MXFP8_E4M3;
+  const size_t eb = mx ? 1 : 2;  // bytes per activation element (E4M3 codes or bf16)
+  L.x_perm = take(TK * H * eb);
+  L.h = take(TK * I * eb);
   L.y_perm = take(TK * H * 4);
   L.s = take(Is ? T * H * 4 : 0);
-  L.h_shared = take(T * Is * 2);
+  L.h_shared = take(T * Is * eb);
   L.x_stage = take(T * H * 2);
   L.logits_stage = take(T * E * 4);
   L.out_stage = take(T * H * 2);
-  L.x_mx = take(c->dtype == MOE_MXFP8_E4M3 ? T * H * 2 : 0);  // MX-rounded x as bf16
+  L.x_mx = take(mx ? T * H : 0);
+  L.x_mx_s = take(mx ? T * H / 32 : 0);
+  L.x_perm_s = take(mx ? TK * H / 32 : 0);
+  L.h_s = take(mx ? TK * I / 32 : 0);
+  L.h_shared_s = take(mx ? T * Is / 32 : 0);
   L.total = off;
   return L;
 }
@@ -116,6 +125,8 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
                           float* y, const uint8_t* sg = nullptr, const uint8_t* su = nullptr,
                           const uint8_t* sd = nullptr) {
   GroupedGemmArgs g;
+  g.a_scale = nullptr;
+  g.h_scale = nullptr;
   g.topk_idx = nullptr;
   g.topk_w = nullptr;
   g.topk = 0;
@@ -211,7 +222,8 @@ MOE_API moe_status_t moe_create(int device, moe_handle_t* out) {
   if (!h) return MOE_ERR_CUDA;
   h->device = device;
   h->num_sms = sms;
-  if (gemm_prepare_device() != cudaSuccess || cudaMalloc(&h->status, 64) != cudaSuccess ||
+  if (gemm_prepare_device() != cudaSuccess || gemm_mx_prepare_device() != cudaSuccess ||
+      cudaMalloc(&h->status, 64) != cudaSuccess ||
       cudaMemset(h->status, 0, 64) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_sh, cudaEventDisableTiming) != cudaSuccess) {
@@ -318,9 +330,11 @@ MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int H, int I, moe
                                                      size_t* bytes) {
   if (!bytes || rows < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  size_t n = align_up((size_t)rows * I * 2 + 1, 256);                         // h
-  if (dtype == MOE_MXFP8_E4M3) n += align_up((size_t)rows * H * 2 + 1, 256);  // dequantised a
-  *bytes = n;
+  (void)H;
+  if (dtype == MOE_MXFP8_E4M3)  // h as E4M3 codes + E8M0 scales
+    *bytes = align_up((size_t)rows * I + 1, 256) + align_up((size_t)rows * (I / 32) + 1, 256);
+  else  // h as bf16
+    *bytes = align_up((size_t)rows * I * 2 + 1, 256);
   return MOE_OK;
 }
 
@@ -348,18 +362,18 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* hbuf = ws;
-  const void* act = a;
-  cudaError_t e = cudaSuccess;
-  if (mx) {  // activations arrive as E4M3 + E8M0: expand them once to exact bf16
-    void* adq = static_cast<uint8_t*>(ws) + align_up((size_t)rows * I * 2 + 1, 256);
-    e = launch_mx_dequantize(static_cast<const uint8_t*>(a), a_scale, rows, H, adq, s);
-    act = adq;
+  GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, a, w_gate, w_up, w_down, ws, y,
+                                mx ? s_gate : nullptr, mx ? s_up : nullptr, mx ? s_down : nullptr);
+  cudaError_t e;
+  if (mx) {  // block-scaled tensor cores; h stays E4M3 + E8M0 between the GEMMs
+    g.a_scale = a_scale;
+    g.h_scale = static_cast<uint8_t*>(ws) + align_up((size_t)rows * I + 1, 256);
+    e = launch_gemm_mx_gate_up(g, s);
+    if (e == cudaSuccess) e = launch_gemm_mx_down(g, s);
+  } else {
+    e = launch_gemm_gate_up(g, s);
+    if (e == cudaSuccess) e = launch_gemm_down(g, s);
   }
-  GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, act, w_gate, w_up, w_down, hbuf,
-                                y, mx ? s_gate : nullptr, mx ? s_up : nullptr, mx ? s_down : nullptr);
-  if (e == cudaSuccess) e = launch_gemm_gate_up(g, s);
-  if (e == cudaSuccess) e = launch_gemm_down(g, s);
   return cuda_status(e);
 }
 
@@ -443,9 +457,11 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   cudaError_t e = cudaSuccess;
   mark(0, sm);
   const void* x_gate = x;  // the router reads x as given (bf16)
-  if (mx) {  // dynamic MXFP8 quantisation of x; the GEMMs take the exact bf16 expansion
+  uint8_t* xq_s = nullptr;  // MXFP8: scales of the quantised x
+  if (mx) {  // dynamic MXFP8 quantisation of x (E4M3 codes + E8M0 scales)
     void* xq = at<void>(ws, L.x_mx);
-    e = launch_mx_quantize(x, T, H, nullptr, nullptr, xq, sm);
+    xq_s = at<uint8_t>(ws, L.x_mx_s);
+    e = launch_mx_quantize(x, T, H, static_cast<uint8_t*>(xq), xq_s, nullptr, sm);
     x = xq;
   }
   cudaStream_t s_sh = ss ? ss : sm;
@@ -458,8 +474,15 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     GroupedGemmArgs g = gemm_args(h, 1, nullptr, T, H, Is, x, w->ws_gate, w->ws_up, w->ws_down,
                                   h_shared, s_out, mx ? w->ss_gate : nullptr,
                                   mx ? w->ss_up : nullptr, mx ? w->ss_down : nullptr);
-    if (e == cudaSuccess) e = launch_gemm_gate_up(g, s_sh);
-    if (e == cudaSuccess) e = launch_gemm_down(g, s_sh);
+    if (mx) {
+      g.a_scale = xq_s;
+      g.h_scale = at<uint8_t>(ws, L.h_shared_s);
+      if (e == cudaSuccess) e = launch_gemm_mx_gate_up(g, s_sh);
+      if (e == cudaSuccess) e = launch_gemm_mx_down(g, s_sh);
+    } else {
+      if (e == cudaSuccess) e = launch_gemm_gate_up(g, s_sh);
+      if (e == cudaSuccess) e = launch_gemm_down(g, s_sh);
+    }
     mark(7, s_sh);
     if (e == cudaSuccess && ss) e = cudaEventRecord(h->ev_sh, ss);  // shared MLP done
   }
@@ -474,14 +497,20 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
                              perm_src, flat_to_perm, h->status, sm);
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, T, H * 2, perm_src, K, TK, x_perm, h->status, sm);
+    e = launch_gather_rows(x, T, mx ? H : H * 2, perm_src, K, TK, x_perm, h->status, sm);
+  if (e == cudaSuccess && mx)
+    e = launch_gather_rows(xq_s, T, H / 32, perm_src, K, TK, at<void>(ws, L.x_perm_s), h->status, sm);
   mark(2, sm);
   GroupedGemmArgs g = gemm_args(h, E, offsets, TK, H, I, x_perm, w->w_gate, w->w_up, w->w_down,
                                 hbuf, y_perm, mx ? w->s_gate : nullptr, mx ? w->s_up : nullptr,
                                 mx ? w->s_down : nullptr);
-  if (e == cudaSuccess) e = launch_gemm_gate_up(g, sm);
+  if (mx) {
+    g.a_scale = at<uint8_t>(ws, L.x_perm_s);
+    g.h_scale = at<uint8_t>(ws, L.h_s);
+  }
+  if (e == cudaSuccess) e = mx ? launch_gemm_mx_gate_up(g, sm) : launch_gemm_gate_up(g, sm);
   mark(3, sm);
-  if (e == cudaSuccess) e = launch_gemm_down(g, sm);
+  if (e == cudaSuccess) e = mx ? launch_gemm_mx_down(g, sm) : launch_gemm_down(g, sm);
   mark(4, sm);
   if (e == cudaSuccess && has_shared && ss) e = cudaStreamWaitEvent(sm, h->ev_sh, 0);
   if (e == cudaSuccess)

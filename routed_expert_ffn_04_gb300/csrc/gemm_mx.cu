@@ -1,0 +1,441 @@
+// Step 3 in MXFP8 on the block-scaled tensor cores: the grouped SwiGLU
+// expert GEMM with E4M3 activations and weights and one E8M0 scale per 32
+// elements along K ("腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战",
+// section 8.2: routed and shared Linears in W8A8 MXFP8). The MMA is
+// tcgen05.mma kind::mxf8f6f4.block_scale: the tensor cores apply the scales,
+// so nothing is expanded to bf16 on the way.
+//
+//   GEMM-1 (MODE 0): h = silu(x Wg^T) * (x Wu^T), re-quantised to MXFP8 per
+//                    32 along I and stored as E4M3 codes + E8M0 scales
+//   GEMM-2 (MODE 1): y = h Wd^T, fp32
+//
+// Persistent, one CTA per SM, 320 threads:
+//   warp 0      TMA producer: each stage is one 128-wide K slice (bytes) of
+//               the 128 token rows (A) and the 128 weight rows (B).
+//   warp 1      TMEM allocator + MMA issuer: 4 MMAs (K = 32 each) per stage.
+//   warps 2..5  epilogue (TMEM -> h codes/scales or staged fp32 y).
+//   warps 6..9  scale staging: per stage, load the E8M0 words of the 128 A
+//               rows and 128 B rows and write them to shared memory as two
+//               32 x 16-byte blocks (row i, word w = scale word of row 32w+i);
+//               the MMA thread copies them into the stage's TMEM scale slot
+//               with tcgen05.cp (warpx4 replication gives exactly the layout
+//               the block-scaled MMA reads, see ptx.cuh) before its MMAs.
+// Tile: M = 128 tokens, N = 128 (GEMM-1: gate 64 + up 64; GEMM-2: 128 of
+// H), double-buffered fp32 accumulators (256 TMEM columns) plus one 8-column
+// scale slot per stage.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+#include "gemm_sched.cuh"
+#include "internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kK = 128;                  // K elements (= bytes) per stage
+constexpr int kStages = 6;
+constexpr int kThreads = 320;
+constexpr int kSfWarp0 = 6;              // scale-writer warps 6..9
+constexpr int kTileBytes = 128 * 128;    // 128 rows x 128 bytes
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kAccCols = 128;
+constexpr int kSfCol0 = 2 * kAccCols;    // scale slot of stage s: kSfCol0 + 8 s (A: +0..3, B: +4..7)
+constexpr int kTmemCols = 512;
+constexpr int kMaxGroups = 1024;
+constexpr int kTableBytes = (kMaxGroups + 8) * 4;
+constexpr int kBarBytes = 256;
+constexpr int kEpiBytes = 4 * 32 * 33 * 4;
+constexpr int kSfBytes = 1024;           // per stage: A block (512 B) + B block (512 B)
+constexpr int kSmem = 1024 + kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes +
+                      kStages * kSfBytes;
+static_assert(kSmem <= 232448, "shared memory budget");
+static_assert(kSfCol0 + 8 * kStages <= kTmemCols, "TMEM budget");
+static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+
+// Four E8M0 scale bytes (K blocks 4kb .. 4kb+3) of one row; rows past the
+// matrix and blocks past the row read as 127 (2^0).
+__device__ __forceinline__ uint32_t scale_word(const uint8_t* s, int row, int rows, int stride, int kb) {
+  if (row >= rows) return 0x7F7F7F7Fu;
+  const uint8_t* p = s + (size_t)row * stride + 4 * kb;
+  if ((stride & 3) == 0) return __ldg(reinterpret_cast<const uint32_t*>(p));
+  uint32_t v = 0;
+  for (int b = 0; b < 4; ++b) v |= (uint32_t)((4 * kb + b < stride) ? __ldg(p + b) : 127) << (8 * b);
+  return v;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_act,
+                           const __grid_constant__ CUtensorMap map_w0,
+                           const __grid_constant__ CUtensorMap map_w1, const KParams p) {
+  constexpr int W_COLS = MODE == 0 ? 64 : 128;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+  uint8_t* base = smem_raw + pad;
+  const uint32_t stage0 = raw_addr + pad;
+  int32_t* tile_start = reinterpret_cast<int32_t*>(base + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + kTableBytes);
+  float* epi_stage = reinterpret_cast<float*>(base + kStages * kStageBytes + kTableBytes + kBarBytes);
+  uint8_t* sf_smem = base + kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes;
+  const uint32_t sf_smem0 = smem_u32(sf_smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_wt = (p.N + W_COLS - 1) / W_COLS;
+  for (int g = threadIdx.x; g < p.G; g += kThreads) {
+    int r0, nr;
+    group_rows(p, g, r0, nr);
+    tile_start[g] = n_wt * ((nr + 127) / 128);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1 + 4);  // producer (with the TMA bytes) + 4 scale writers
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_act);
+    prefetch_tensormap(&map_w0);
+    prefetch_tensormap(&map_w1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the per-group tile counts
+    const int per = (p.G + 31) / 32;
+    const int b = lane * per;
+    const int e = (b + per < p.G) ? b + per : p.G;
+    int local = 0;
+    for (int g = b; g < e; ++g) local += tile_start[g];
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int g = b; g < e; ++g) {
+      const int c = tile_start[g];
+      tile_start[g] = run;
+      run += c;
+    }
+    if (lane == 31) tile_start[p.G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tile_start[p.G];
+  const int n_k = (p.num_kb + 1) / 2;  // p.num_kb counts 64-wide slices; a stage holds two
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_normal();
+      Ring rg;
+      Armed armed;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<128>(p, tile_start, tile);
+        const int act_row = ti.row0 + ti.tt * 128;
+        const int w_row0 = ti.g * p.N + ti.wt * W_COLS;
+        const int w_row1 = MODE == 0 ? w_row0 : w_row0 + 64;
+        for (int kb = 0; kb < n_k; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
+                                 MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(rg.s);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t st = stage0 + rg.s * kStageBytes;
+          const int kx = kb * kK;
+          tma_load_2d(st, &map_act, fb, kx, act_row);
+          tma_load_2d_hint(st + kTileBytes, &map_w0, fb, kx, w_row0, pol);
+          tma_load_2d_hint(st + kTileBytes + kTileBytes / 2, &map_w1, fb, kx, w_row1, pol);
+          armed.mark(rg);
+          rg.next(kStages);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (armed.mask & (1u << s)) drain_wait(full_bar(s), (armed.phase >> s) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      Ring rg;
+      bool ok = true, issued = false;
+      int local = 0;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t ap = (uint32_t)(local >> 1) & 1u;
+        if (!mbar_wait_bounded(tempty_bar(acc), ap ^ 1u, abort_flag, p.status,
+                               MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+        for (int kb = 0; kb < n_k; ++kb) {
+          if (!mbar_wait_bounded(full_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
+                                 p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = stage0 + rg.s * kStageBytes;
+          const uint32_t sf = tmem_base + (uint32_t)(kSfCol0 + 8 * rg.s);
+          tmem_cp_32x128b_warpx4(sf, sf_smem0 + rg.s * kSfBytes);
+          tmem_cp_32x128b_warpx4(sf + 4, sf_smem0 + rg.s * kSfBytes + 512);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            umma_mxf8(d, sw128_kmajor_desc(st + k * 32), sw128_kmajor_desc(st + kTileBytes + k * 32),
+                      idesc_mxf8_e4m3(128, 128, k, k), sf, sf + 4, (kb | k) ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit(empty_bar(rg.s));
+          rg.next(kStages);
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+      }
+      if (!ok && issued) {
+        umma_commit(drain_bar);
+        drain_wait(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else if (warp < kSfWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    float* stg = epi_stage + q * 32 * 33;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t ap = (uint32_t)(local >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(tfull_bar(acc), ap, abort_flag, p.status, MOE_DEV_TIMEOUT_EPILOGUE,
+                               p.limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const TileInfo ti = decode_tile<128>(p, tile_start, tile);
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
+      const int r = ti.tt * 128 + q * 32 + lane;
+      const bool rv = r < ti.nrows;
+      if (MODE == 0) {
+        // h = silu(gate) * up for columns 0..63 (gate) / 64..127 (up), MXFP8 per 32.
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32x32b_x32(tb + c, g);
+          tmem_ld_32x32b_x32(tb + 64 + c, u);
+          tmem_ld_wait();
+          const int col = ti.wt * 64 + c;
+          if (rv && col < p.N) {
+            float hv[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              hv[j] = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+              amax = fmaxf(amax, fabsf(hv[j]));
+            }
+            uint32_t w[8];
+            int code = 0;
+            if (amax == 0.0f) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = 0u;
+            } else {
+              const int sexp = mx_shared_exp(amax);
+              code = sexp + 127;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                w[j] = mx_encode(hv[4 * j], sexp) | (mx_encode(hv[4 * j + 1], sexp) << 8) |
+                       (mx_encode(hv[4 * j + 2], sexp) << 16) | (mx_encode(hv[4 * j + 3], sexp) << 24);
+            }
+            const size_t row = (size_t)(ti.row0 + r);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.N + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            p.out_scale[row * (p.N / 32) + col / 32] = (uint8_t)code;
+          }
+        }
+      } else {
+        const int r_first = ti.tt * 128 + q * 32;
+        float* y = static_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c, v);
+          tmem_ld_wait();
+          const int col = ti.wt * 128 + c;
+          if (col < p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
+            __syncwarp();
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr) {
+              const int row = r_first + rr;
+              if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+            }
+            __syncwarp();
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+  } else {
+    // ------------------------------------------------------------ scale writers
+    // Warp w (0..3 here) handles A row and B row 32w + lane: their scale
+    // words go to byte 16 lane + 4 w of the stage's A and B blocks.
+    const int q = warp - kSfWarp0;
+    auto load_words = [&](int tile, int kb, uint32_t& wa, uint32_t& wb) {
+      const TileInfo ti = decode_tile<128>(p, tile_start, tile);
+      const int m = q * 32 + lane;
+      const int act_row = ti.row0 + ti.tt * 128 + m;
+      wa = (ti.tt * 128 + m < ti.nrows) ? scale_word(p.s_act, act_row, p.rows, p.sstride, kb)
+                                         : 0x7F7F7F7Fu;
+      const int w_row0 = ti.g * p.N + ti.wt * W_COLS;
+      const int w_row1 = MODE == 0 ? w_row0 : w_row0 + 64;
+      wb = m < 64 ? scale_word(p.s_w0, w_row0 + m, p.w_rows, p.sstride, kb)
+                  : scale_word(p.s_w1, w_row1 + m - 64, p.w_rows, p.sstride, kb);
+    };
+    // Scale words are loaded kPre stages ahead into a small register ring.
+    constexpr int kPre = 4;
+    int cur_tile = blockIdx.x, cur_kb = 0, pre_tile = blockIdx.x, pre_kb = 0;
+    auto advance = [&](int& t, int& k) {
+      if (++k == n_k) {
+        k = 0;
+        t += gridDim.x;
+      }
+    };
+    uint32_t qa[kPre], qb[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      qa[i] = 0x7F7F7F7Fu;
+      qb[i] = 0x7F7F7F7Fu;
+      if (pre_tile < total) load_words(pre_tile, pre_kb, qa[i], qb[i]);
+      advance(pre_tile, pre_kb);
+    }
+    Ring rg;
+    bool ok = true;
+    while (ok && cur_tile < total) {
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        if (!ok || cur_tile >= total) break;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
+                                  MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint32_t* blk = reinterpret_cast<uint32_t*>(sf_smem + rg.s * kSfBytes);
+        blk[lane * 4 + q] = qa[i];
+        blk[128 + lane * 4 + q] = qb[i];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_bar(rg.s));
+        rg.next(kStages);
+        if (pre_tile < total) load_words(pre_tile, pre_kb, qa[i], qb[i]);
+        advance(pre_tile, pre_kb);
+        advance(cur_tile, cur_kb);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int MODE>
+cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
+  const int Kdim = MODE == 0 ? a.H : a.I;
+  const int N = MODE == 0 ? a.I : a.H;
+  const void* act = MODE == 0 ? a.a : a.h;
+  const uint8_t* act_scale = MODE == 0 ? a.a_scale : a.h_scale;
+  const void* w0 = MODE == 0 ? a.w_gate : a.w_down;
+  const void* w1 = MODE == 0 ? a.w_up : a.w_down;
+  if (a.rows == 0 || a.G == 0) return cudaSuccess;
+  const int G = a.offsets ? a.G : 1;
+  CUtensorMap m_act, m_w0, m_w1;
+  if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) ||
+      !make_tmap_u8(&m_w0, w0, Kdim, (uint64_t)G * N, 64) ||
+      !make_tmap_u8(&m_w1, w1, Kdim, (uint64_t)G * N, 64))
+    return cudaErrorInvalidValue;
+  KParams p = {};
+  p.offsets = a.offsets;
+  p.G = G;
+  p.rows = a.rows;
+  p.num_kb = (Kdim + 63) / 64;
+  p.N = N;
+  p.out = MODE == 0 ? a.h : static_cast<void*>(a.y);
+  p.status = a.status;
+  p.limit_ns = a.wait_limit_ns;
+  p.s_w0 = MODE == 0 ? a.s_gate : a.s_down;
+  p.s_w1 = MODE == 0 ? a.s_up : a.s_down;
+  p.sstride = Kdim / 32;
+  p.w_rows = G * N;
+  p.s_act = act_scale;
+  p.out_scale = MODE == 0 ? a.h_scale : nullptr;
+  constexpr int W_COLS = MODE == 0 ? 64 : 128;
+  const long long n_wt = (N + W_COLS - 1) / W_COLS;
+  const long long max_tiles = n_wt * ((a.rows + 127) / 128 + G);
+  const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
+  grouped_gemm_mx_kernel<MODE><<<grid, kThreads, kSmem, s>>>(m_act, m_w0, m_w1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_mx_prepare_device() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<0>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem);
+  return e;
+}
+
+cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
+  return run_gemm_mx<0>(a, s);
+}
+
+cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s) {
+  return run_gemm_mx<1>(a, s);
+}
+
+}  // namespace moe

@@ -2,6 +2,7 @@
 // translation units. Host-side only; nothing here is exported.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -54,6 +55,8 @@ struct GroupedGemmArgs {
   int route_norm;
   int mode;                // GemmMode
   int mx;                  // 1: weights are E4M3 + E8M0/32 (h MX-rounded too)
+  const uint8_t* a_scale;  // native MXFP8: E8M0 scales of `a` [rows, H/32] (a holds E4M3 codes)
+  uint8_t* h_scale;        // native MXFP8: E8M0 scales of h [rows, I/32] (h holds E4M3 codes)
   const uint8_t* s_gate;   // MX scales [G*I, H/32], [G*I, H/32], [G*H, I/32]
   const uint8_t* s_up;
   const uint8_t* s_down;
@@ -65,6 +68,13 @@ bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailab
 // Opt the GEMM kernels into their dynamic shared memory on the current device
 // (once per device, outside any stream capture).
 cudaError_t gemm_prepare_device();
+// 2-D uint8 tensor map [outer, inner], box {128 bytes, box_rows}, 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
+// Native MXFP8 grouped GEMM (gemm_mx.cu): block-scaled tcgen05 MMA, E4M3
+// activations (a + a_scale; GEMM-2 reads h + h_scale) and weights.
+cudaError_t gemm_mx_prepare_device();
+cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
 // Gating GEMM (one group, E <= 256) with routing in its epilogue: a.h = x

@@ -156,6 +156,61 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with E4M3 A and B and one E8M0
+// scale per 32 elements of K (kind::mxf8f6f4, block_scale, scale_vec::1X),
+// fp32 accumulator; K = 32 per instruction. Scale layout in TMEM (M = 128):
+// A row m at lane m, column sfa + m/32; B row n at lane 32*(quarter) + n%32,
+// column sfb + n/32 in every lane quarter; the byte of each 32-bit word is
+// chosen by the scale ids in the instruction descriptor.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B (K-major),
+// UE8M0 scales, fp32 D; scale ids select the byte of the scale words.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int a_sf_id, int b_sf_id) {
+  return ((uint32_t)b_sf_id << 4)          // B scale id
+         | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | (1u << 23)                     // scale format: UE8M0
+         | ((uint32_t)(M >> 4) << 24)     // M / 16
+         | ((uint32_t)a_sf_id << 29);     // A scale id
+}
+
+// Copy a 32-row x 16-byte shared-memory block (row i at byte 16 i) into TMEM
+// lanes 0..31, columns taddr..taddr+3, replicated into all four lane quarters
+// (32x128b.warpx4). Issued by the MMA thread, so it is ordered before that
+// thread's following tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address >> 4
+  d |= (uint64_t)(16 >> 4) << 16;                // leading byte offset (one 16-byte column)
+  d |= (uint64_t)(128 >> 4) << 32;               // stride byte offset: 8 rows x 16 bytes
+  d |= (uint64_t)1 << 46;                        // descriptor version (tcgen05)
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
+// One 32-bit value per lane into this warp's lane quarter, at column taddr (x1),
+// or four consecutive columns (x4).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
