@@ -74,7 +74,8 @@ typedef enum {
  * (0 = no shared expert). scaling = router_scaling_factor ([Hy3] section 一:
  * 2.826); route_norm != 0 divides the K sigmoid scores by their sum.
  * Limits: 1 <= K <= min(E, 32), E <= 1024, H % 64 == 0, I % 64 == 0,
- * I_shared % 64 == 0, T * K < 2^31, T*max(H,I) < 2^31. */
+ * I_shared % 64 == 0 (MXFP8: H, I, I_shared % 128 == 0), T * K < 2^31,
+ * T*K*max(H,I) < 2^40. */
 typedef struct {
   int T, H, E, K, I, I_shared;
   float scaling;
@@ -83,10 +84,15 @@ typedef struct {
 } moe_config_t;
 
 /* Layer weights (device). bf16 mode: w_* are bf16, s_* ignored.
- * MXFP8 mode: w_* are E4M3 codes (uint8) and s_* the E8M0 scales, one per
- * 32 consecutive elements of a row ([rows, cols/32]).
  *   w_gate, w_up: [E, I, H]     w_down: [E, H, I]
- *   ws_gate, ws_up: [I_shared, H]   ws_down: [H, I_shared]  (NULL if I_shared == 0) */
+ *   ws_gate, ws_up: [I_shared, H]   ws_down: [H, I_shared]  (NULL if I_shared == 0)
+ * MXFP8 mode: w_* are E4M3 codes (uint8) and the E8M0 scales (one per 32
+ * consecutive elements of a row) are given as scale atoms, the layout the
+ * block-scaled tensor cores read, written by moe_pack_mx_scales:
+ *   s_gate  = atoms of gate and up together (moe_pack_mx_scales(gate, up)),
+ *   s_down  = atoms of down (moe_pack_mx_scales(down, NULL)),
+ *   s_up    unused (NULL); ss_gate, ss_up, ss_down the same for the shared
+ *   expert. Every scale pointer 16-byte aligned. */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
   const uint8_t *s_gate, *s_up, *s_down;
@@ -164,22 +170,27 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
                                  void* x_perm, uint8_t* x_perm_scale, void* ws, size_t ws_bytes,
                                  moe_stream_t stream);
 
-/* Scratch bytes moe_grouped_swiglu_gemm needs: the [rows, I] bf16
- * intermediate, plus (MXFP8) the [rows, H] bf16 expansion of `a`. */
-MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int H, int I, moe_dtype_t dtype,
-                                                     size_t* bytes);
+/* Scratch bytes moe_grouped_swiglu_gemm needs for `rows` rows in
+ * `num_groups` groups: the [rows, I] intermediate (bf16, or MXFP8 E4M3 codes
+ * plus the scale atoms of h and of `a`, one atom row-block per 128 rows of
+ * each group). */
+MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int num_groups, int H, int I,
+                                                     moe_dtype_t dtype, size_t* bytes);
 
 /* Step 3, the grouped expert GEMM with SwiGLU (the grouped GMM of [Hy3]
  * section 8.5): for each group g, rows offsets[g] .. offsets[g+1]-1 of `a`:
  *   h = silu(a W_gate[g]^T) * (a W_up[g]^T)   (fp32 accumulate, h stored bf16
  *                                              or, in MXFP8 mode, re-quantised)
  *   y = h W_down[g]^T                          (fp32 accumulate, stored fp32)
- * a (device): [rows, H] bf16 (MXFP8: E4M3 codes + a_scale [rows, H/32] E8M0).
- * MXFP8: w_* are E4M3 codes and s_gate, s_up: [num_groups*I, H/32],
- *   s_down: [num_groups*H, I/32] their E8M0 scales; h is rounded to MXFP8
- *   (blocks of 32 along I) before GEMM-2, as the W8A8 path quantises every
- *   Linear input ([Hy3] section 8.2). The weights stream from HBM as E4M3 and
- *   are expanded exactly to bf16 in shared memory for the tensor cores.
+ * a (device): [rows, H] bf16 (MXFP8: E4M3 codes + a_scale [rows, H/32] E8M0,
+ *   row-major).
+ * MXFP8: w_* are E4M3 codes; s_gate = moe_pack_mx_scales(gate, up) atoms of
+ *   the [num_groups*I, H/32] gate and up scales, s_down =
+ *   moe_pack_mx_scales(down, NULL) atoms of the [num_groups*H, I/32] down
+ *   scales, s_up unused. h is rounded to MXFP8 (blocks of 32 along I) before
+ *   GEMM-2, as the W8A8 path quantises every Linear input ([Hy3] section
+ *   8.2). Operands and scales go to the block-scaled tensor cores as stored.
+ *   H % 128 == 0, I % 128 == 0.
  * offsets (device): [num_groups + 1] int32, non-decreasing, offsets[0] = 0,
  *   offsets[num_groups] <= rows; NULL means one group of all rows (a dense
  *   SwiGLU MLP, used for the shared expert).
@@ -214,14 +225,30 @@ MOE_API moe_status_t moe_combine(moe_handle_t h, const moe_config_t* cfg, const 
 MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream);
 
+/* Scale atoms for the block-scaled MXFP8 GEMM from row-major E8M0 scales
+ * (as moe_quantize_mxfp8 writes them). An atom holds the scales of 128 rows
+ * x 128 elements (4 per row) in 512 bytes: row r of the block, K-block j at
+ * byte 16 (r % 32) + 4 (r / 32) + j; the atoms of a matrix follow each other
+ * row-block major (128-row block b, K-block a at atom b * cols/128 + a).
+ * scale1 == NULL: atoms of scale0 [rows, cols/32], rows % 128 == 0.
+ * scale1 != NULL: gate (scale0) and up (scale1) scales, each [rows, cols/32]
+ *   with rows % 64 == 0, interleaved per 64 rows (gate rows 0-63, up rows
+ *   0-63, gate rows 64-127, ...) into a 2*rows-row atom matrix: the row order
+ *   of one GEMM-1 tile. Use it for the per-expert [E*I] gate/up pair.
+ * cols % 128 == 0. atoms (device): rows * cols / 32 bytes (twice that with
+ * scale1). Pointers 16-byte aligned. Packing is a one-time weight step. */
+MOE_API moe_status_t moe_pack_mx_scales(moe_handle_t h, const uint8_t* scale0,
+                                        const uint8_t* scale1, int64_t rows, int cols,
+                                        uint8_t* atoms, moe_stream_t stream);
+
 /* The whole layer, steps 1-4 plus the shared expert, with the two-stream
  * orchestration of [Hy3] section 8.5 / [HyI3] §3: an event recorded on
  * `main` at entry is waited on by `side`, which runs the shared expert and
  * records a second event that `main` waits on before the combine.
  * side == NULL runs the shared expert on `main` before the routed path.
  * x (device): [T, H] bf16 (MXFP8 mode: quantised inside, per call, with the
- * rule of moe_quantize_mxfp8; weights must then be E4M3 + scales, for
- * example from moe_quantize_mxfp8 on the bf16 weights, and H % 128 == 0).
+ * rule of moe_quantize_mxfp8; weights must then be E4M3 codes + scale atoms,
+ * for example moe_quantize_mxfp8 on the bf16 weights then moe_pack_mx_scales).
  * logits (device): [T, E] fp32. out (device): [T, H] bf16.
  * ws (device): at least moe_workspace_size bytes. */
 MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,

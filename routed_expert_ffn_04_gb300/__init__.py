@@ -75,10 +75,11 @@ def load(build_if_missing: bool = False):
         "moe_route": [P, P, P, P, P, P],
         "moe_permute_workspace_size": [P, PS],
         "moe_permute": [P, P, P, P, P, P, P, P, P, P, P, P, S, P],
-        "moe_grouped_gemm_workspace_size": [I, I, I, I, PS],
+        "moe_grouped_gemm_workspace_size": [I, I, I, I, I, PS],
         "moe_grouped_swiglu_gemm": [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, S, P],
         "moe_combine": [P, P, P, P, P, P, P, P],
         "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
+        "moe_pack_mx_scales": [P, P, P, ctypes.c_int64, I, P, P],
         "moe_layer_forward": [P, P, P, P, P, P, P, S, P, P],
         "moe_layer_forward_host": [P, P, P, P, P, P, P, S, P, P],
         "moe_get_device_status": [P, ctypes.POINTER(I), P],
@@ -136,10 +137,10 @@ def permute_workspace_size(cfg: Config) -> int:
     return n.value
 
 
-def grouped_gemm_workspace_size(rows: int, H: int, I: int, dtype: int = MOE_BF16) -> int:
+def grouped_gemm_workspace_size(rows: int, H: int, I: int, dtype: int = MOE_BF16, num_groups: int = 1) -> int:
     n = ctypes.c_size_t(0)
-    _check(load().moe_grouped_gemm_workspace_size(int(rows), int(H), int(I), int(dtype), ctypes.byref(n)),
-           "moe_grouped_gemm_workspace_size")
+    _check(load().moe_grouped_gemm_workspace_size(int(rows), int(num_groups), int(H), int(I), int(dtype),
+                                                  ctypes.byref(n)), "moe_grouped_gemm_workspace_size")
     return n.value
 
 
@@ -239,12 +240,36 @@ def quantize_mx(h: Handle, t, stream=None):
 
 
 def quantize_weights_mx(h: Handle, w: dict, stream=None) -> dict:
-    """MX form of a bf16 weight dict: w_* -> E4M3 codes, s_* / ss_* -> scales."""
+    """MX form of a bf16 weight dict: w_* -> E4M3 codes, s_* / ss_* -> row-major scales."""
     out = {}
     for k, v in w.items():
         q, sc = quantize_mx(h, v, stream=stream)
         out[k] = q
         out[("ss_" + k[3:]) if k.startswith("ws_") else ("s_" + k[2:])] = sc
+    return out
+
+
+def pack_mx_scales(h: Handle, scale0, scale1=None, stream=None):
+    """Scale atoms (moe_pack_mx_scales) of row-major E8M0 scales [..., cols/32]:
+    of scale0 alone, or of the gate (scale0) / up (scale1) pair."""
+    rows = scale0.numel() // scale0.shape[-1]
+    cols = scale0.shape[-1] * 32
+    out = torch.empty(scale0.numel() * (2 if scale1 is not None else 1), dtype=torch.uint8, device=scale0.device)
+    _check(load().moe_pack_mx_scales(h.ptr, _p(scale0), _p(scale1), int(rows), int(cols), _p(out), _stream(stream)),
+           "moe_pack_mx_scales")
+    return out
+
+
+def pack_weights_mx(h: Handle, mx: dict, stream=None) -> dict:
+    """Codes + row-major scales (quantize_weights_mx) -> the weight form the
+    MXFP8 layer takes: s_gate / ss_gate = gate+up atoms, s_down / ss_down =
+    down atoms, s_up / ss_up dropped."""
+    out = {k: v for k, v in mx.items() if not k.startswith("s")}
+    for p in ("s_", "ss_"):
+        if mx.get(p + "gate") is None:
+            continue
+        out[p + "gate"] = pack_mx_scales(h, mx[p + "gate"], mx[p + "up"], stream=stream)
+        out[p + "down"] = pack_mx_scales(h, mx[p + "down"], stream=stream)
     return out
 
 
@@ -295,8 +320,11 @@ class MoELayer:
                                shape.route_norm, MOE_MXFP8_E4M3 if shape.dtype == "mxfp8" else MOE_BF16)
         self.handle = Handle(self.device.index)
         self.ws = torch.empty(workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
-        if shape.dtype == "mxfp8" and weights["w_gate"].dtype != torch.uint8:
-            weights = quantize_weights_mx(self.handle, weights)
+        if shape.dtype == "mxfp8":
+            if weights["w_gate"].dtype != torch.uint8:
+                weights = quantize_weights_mx(self.handle, weights)
+            if weights.get("s_up") is not None:  # row-major scales -> scale atoms
+                weights = pack_weights_mx(self.handle, weights)
             torch.cuda.synchronize(self.device)
         self.weights_t = weights
         self.weights = make_weights(weights)

@@ -58,7 +58,9 @@ moe_status_t check_cfg(const moe_config_t* c) {
   const long long wide = c->H > c->I ? c->H : c->I;
   if ((long long)c->T * c->K * wide >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  if (c->dtype == MOE_MXFP8_E4M3 && c->H % 128) return MOE_ERR_INVALID_ARG;  // scale rows in 4-byte units
+  // MXFP8: whole scale atoms (128 x 128) along H, I and I_shared.
+  if (c->dtype == MOE_MXFP8_E4M3 && (c->H % 128 || c->I % 128 || c->I_shared % 128))
+    return MOE_ERR_INVALID_ARG;
   if (!(c->scaling == c->scaling)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -67,9 +69,9 @@ moe_status_t check_cfg(const moe_config_t* c) {
 struct Layout {
   size_t topk_idx, topk_w, counts, offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
       y_perm, s, h_shared, x_stage, logits_stage, out_stage, x_mx, total;
-  // MXFP8 only: E8M0 scales of x (x_mx holds its E4M3 codes), of the permuted
-  // x, of h and of the shared expert's h.
-  size_t x_mx_s, x_perm_s, h_s, h_shared_s;
+  // MXFP8 only: E8M0 scales of x (x_mx holds its E4M3 codes) row-major and
+  // as scale atoms; atoms of the permuted x, of h and of the shared expert's h.
+  size_t x_mx_s, x_mx_atoms, x_perm_s, h_s, h_shared_s;
 };
 
 Layout layout_of(const moe_config_t* c) {
@@ -100,9 +102,10 @@ Layout layout_of(const moe_config_t* c) {
   L.out_stage = take(T * H * 2);
   L.x_mx = take(mx ? T * H : 0);
   L.x_mx_s = take(mx ? T * H / 32 : 0);
-  L.x_perm_s = take(mx ? TK * H / 32 : 0);
-  L.h_s = take(mx ? TK * I / 32 : 0);
-  L.h_shared_s = take(mx ? T * Is / 32 : 0);
+  L.x_mx_atoms = take(mx ? scale_atom_bytes(T, 1, (int)H) : 0);
+  L.x_perm_s = take(mx ? scale_atom_bytes(TK, (int)E, (int)H) : 0);
+  L.h_s = take(mx ? scale_atom_bytes(TK, (int)E, (int)I) : 0);
+  L.h_shared_s = take(mx ? scale_atom_bytes(T, 1, (int)Is) : 0);
   L.total = off;
   return L;
 }
@@ -326,15 +329,26 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
   return cuda_status(e);
 }
 
-MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int H, int I, moe_dtype_t dtype,
-                                                     size_t* bytes) {
-  if (!bytes || rows < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+namespace {
+// moe_grouped_swiglu_gemm workspace: h, then (MXFP8) the scale atoms of h and of a.
+struct GemmWs {
+  size_t h, h_atoms, a_atoms, total;
+};
+GemmWs gemm_ws(int rows, int groups, int H, int I, bool mx) {
+  GemmWs L;
+  L.h = 0;
+  L.h_atoms = align_up((size_t)rows * I * (mx ? 1 : 2) + 1, 256);
+  L.a_atoms = L.h_atoms + (mx ? align_up(scale_atom_bytes(rows, groups, I) + 1, 256) : 0);
+  L.total = L.a_atoms + (mx ? align_up(scale_atom_bytes(rows, groups, H) + 1, 256) : 0);
+  return L;
+}
+}  // namespace
+
+MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int num_groups, int H, int I,
+                                                     moe_dtype_t dtype, size_t* bytes) {
+  if (!bytes || rows < 0 || num_groups <= 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  (void)H;
-  if (dtype == MOE_MXFP8_E4M3)  // h as E4M3 codes + E8M0 scales
-    *bytes = align_up((size_t)rows * I + 1, 256) + align_up((size_t)rows * (I / 32) + 1, 256);
-  else  // h as bf16
-    *bytes = align_up((size_t)rows * I * 2 + 1, 256);
+  *bytes = gemm_ws(rows, num_groups, H, I, dtype == MOE_MXFP8_E4M3).total;
   return MOE_OK;
 }
 
@@ -352,23 +366,26 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
   const bool mx = dtype == MOE_MXFP8_E4M3;
   if (!a || !w_gate || !w_up || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
-  if (mx && (!a_scale || !s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {a, offsets, w_gate, w_up, w_down, y, ws};
+  if (mx && (!a_scale || !s_gate || !s_down || H % 128 || I % 128)) return MOE_ERR_INVALID_ARG;
+  (void)s_up;  // MXFP8: s_gate holds the gate and up scale atoms together
+  const void* ptrs[] = {a, offsets, w_gate, w_up, w_down, y, ws, s_gate, s_down};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
-  size_t need = 0;
-  moe_grouped_gemm_workspace_size(rows, H, I, dtype, &need);
-  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  const GemmWs W = gemm_ws(rows, num_groups, H, I, mx);
+  if (ws_bytes < W.total) return MOE_ERR_WORKSPACE;
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, a, w_gate, w_up, w_down, ws, y,
-                                mx ? s_gate : nullptr, mx ? s_up : nullptr, mx ? s_down : nullptr);
-  cudaError_t e;
+                                mx ? s_gate : nullptr, nullptr, mx ? s_down : nullptr);
+  cudaError_t e = cudaSuccess;
   if (mx) {  // block-scaled tensor cores; h stays E4M3 + E8M0 between the GEMMs
-    g.a_scale = a_scale;
-    g.h_scale = static_cast<uint8_t*>(ws) + align_up((size_t)rows * I + 1, 256);
-    e = launch_gemm_mx_gate_up(g, s);
+    uint8_t* a_atoms = at<uint8_t>(ws, W.a_atoms);
+    e = launch_gather_scale_atoms(a_scale, rows, H, nullptr, 1, offsets, num_groups, rows, a_atoms,
+                                  h->status, s);
+    g.a_scale = a_atoms;
+    g.h_scale = at<uint8_t>(ws, W.h_atoms);
+    if (e == cudaSuccess) e = launch_gemm_mx_gate_up(g, s);
     if (e == cudaSuccess) e = launch_gemm_mx_down(g, s);
   } else {
     e = launch_gemm_gate_up(g, s);
@@ -391,6 +408,19 @@ MOE_API moe_status_t moe_combine(moe_handle_t h, const moe_config_t* cfg, const 
                                     cfg->H, out, h->status, static_cast<cudaStream_t>(stream)));
 }
 
+MOE_API moe_status_t moe_pack_mx_scales(moe_handle_t h, const uint8_t* scale0,
+                                        const uint8_t* scale1, int64_t rows, int cols,
+                                        uint8_t* atoms, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128) return MOE_ERR_INVALID_ARG;
+  if (rows % (scale1 ? 64 : 128)) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!scale0 || !atoms)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(scale0) || !aligned16(scale1) || !aligned16(atoms)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_handle(h);
+  if (st != MOE_OK) return st;
+  return cuda_status(
+      launch_pack_weight_scales(scale0, scale1, rows, cols, atoms, static_cast<cudaStream_t>(stream)));
+}
+
 MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
@@ -399,7 +429,8 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
   return cuda_status(
-      launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr, static_cast<cudaStream_t>(stream)));
+      launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr, nullptr,
+                         static_cast<cudaStream_t>(stream)));
 }
 
 static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
@@ -415,8 +446,11 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
   const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
-  if (mx && (!w->s_gate || !w->s_up || !w->s_down)) return MOE_ERR_INVALID_ARG;
-  if (mx && has_shared && (!w->ss_gate || !w->ss_up || !w->ss_down)) return MOE_ERR_INVALID_ARG;
+  if (mx && (!w->s_gate || !w->s_down)) return MOE_ERR_INVALID_ARG;
+  if (mx && has_shared && (!w->ss_gate || !w->ss_down)) return MOE_ERR_INVALID_ARG;
+  if (mx && (!aligned16(w->s_gate) || !aligned16(w->s_down) || !aligned16(w->ss_gate) ||
+             !aligned16(w->ss_down)))
+    return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, logits, out, ws, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -461,7 +495,8 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (mx) {  // dynamic MXFP8 quantisation of x (E4M3 codes + E8M0 scales)
     void* xq = at<void>(ws, L.x_mx);
     xq_s = at<uint8_t>(ws, L.x_mx_s);
-    e = launch_mx_quantize(x, T, H, static_cast<uint8_t*>(xq), xq_s, nullptr, sm);
+    e = launch_mx_quantize(x, T, H, static_cast<uint8_t*>(xq), xq_s,
+                           has_shared ? at<uint8_t>(ws, L.x_mx_atoms) : nullptr, nullptr, sm);
     x = xq;
   }
   cudaStream_t s_sh = ss ? ss : sm;
@@ -472,10 +507,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     }
     mark(6, s_sh);
     GroupedGemmArgs g = gemm_args(h, 1, nullptr, T, H, Is, x, w->ws_gate, w->ws_up, w->ws_down,
-                                  h_shared, s_out, mx ? w->ss_gate : nullptr,
-                                  mx ? w->ss_up : nullptr, mx ? w->ss_down : nullptr);
+                                  h_shared, s_out, mx ? w->ss_gate : nullptr, nullptr,
+                                  mx ? w->ss_down : nullptr);
     if (mx) {
-      g.a_scale = xq_s;
+      g.a_scale = at<uint8_t>(ws, L.x_mx_atoms);
       g.h_scale = at<uint8_t>(ws, L.h_shared_s);
       if (e == cudaSuccess) e = launch_gemm_mx_gate_up(g, s_sh);
       if (e == cudaSuccess) e = launch_gemm_mx_down(g, s_sh);
@@ -499,10 +534,11 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (e == cudaSuccess)
     e = launch_gather_rows(x, T, mx ? H : H * 2, perm_src, K, TK, x_perm, h->status, sm);
   if (e == cudaSuccess && mx)
-    e = launch_gather_rows(xq_s, T, H / 32, perm_src, K, TK, at<void>(ws, L.x_perm_s), h->status, sm);
+    e = launch_gather_scale_atoms(xq_s, T, H, perm_src, K, offsets, E, TK,
+                                  at<uint8_t>(ws, L.x_perm_s), h->status, sm);
   mark(2, sm);
   GroupedGemmArgs g = gemm_args(h, E, offsets, TK, H, I, x_perm, w->w_gate, w->w_up, w->w_down,
-                                hbuf, y_perm, mx ? w->s_gate : nullptr, mx ? w->s_up : nullptr,
+                                hbuf, y_perm, mx ? w->s_gate : nullptr, nullptr,
                                 mx ? w->s_down : nullptr);
   if (mx) {
     g.a_scale = at<uint8_t>(ws, L.x_perm_s);

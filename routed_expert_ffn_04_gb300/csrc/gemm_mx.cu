@@ -9,17 +9,19 @@
 //                    32 along I and stored as E4M3 codes + E8M0 scales
 //   GEMM-2 (MODE 1): y = h Wd^T, fp32
 //
-// Persistent, one CTA per SM, 320 threads:
-//   warp 0      TMA producer: each stage is one 128-wide K slice (bytes) of
-//               the 128 token rows (A) and the 128 weight rows (B).
-//   warp 1      TMEM allocator + MMA issuer: 4 MMAs (K = 32 each) per stage.
-//   warps 2..5  epilogue (TMEM -> h codes/scales or staged fp32 y).
-//   warps 6..9  scale staging: per stage, load the E8M0 words of the 128 A
-//               rows and 128 B rows and write them to shared memory as two
-//               32 x 16-byte blocks (row i, word w = scale word of row 32w+i);
-//               the MMA thread copies them into the stage's TMEM scale slot
-//               with tcgen05.cp (warpx4 replication gives exactly the layout
-//               the block-scaled MMA reads, see ptx.cuh) before its MMAs.
+// Scales travel in scale atoms (mx_layout.cuh): 512 bytes per 128 rows x 128
+// K elements, already in the order the block-scaled MMA reads from TMEM.
+// A stage's two atoms (A rows, B rows) ride on the same mbarrier as its TMA
+// tiles, and the MMA thread moves them into TMEM with tcgen05.cp.
+//
+// Persistent, one CTA per SM, 192 threads:
+//   warp 0      producer: per stage, the 128-wide K slice (bytes) of the 128
+//               token rows (A) and 128 weight rows (B) by TMA, plus the two
+//               scale atoms by bulk copy.
+//   warp 1      TMEM allocator + MMA issuer: per stage two tcgen05.cp
+//               (32x128b.warpx4: one 32 x 16-byte atom block replicated into
+//               the four lane quarters) and 4 MMAs (K = 32 each).
+//   warps 2..5  epilogue (TMEM -> h codes + scale atoms, or staged fp32 y).
 // Tile: M = 128 tokens, N = 128 (GEMM-1: gate 64 + up 64; GEMM-2: 128 of
 // H), double-buffered fp32 accumulators (256 TMEM columns) plus one 8-column
 // scale slot per stage.
@@ -32,6 +34,7 @@
 #include "gemm_sched.cuh"
 #include "internal.h"
 #include "mx.cuh"
+#include "mx_layout.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -39,10 +42,10 @@ namespace {
 
 constexpr int kK = 128;                  // K elements (= bytes) per stage
 constexpr int kStages = 6;
-constexpr int kThreads = 320;
-constexpr int kSfWarp0 = 6;              // scale-writer warps 6..9
+constexpr int kThreads = 192;
 constexpr int kTileBytes = 128 * 128;    // 128 rows x 128 bytes
 constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kSfBytes = 2 * kAtomBytes; // per stage: A atom + B atom
 constexpr int kAccCols = 128;
 constexpr int kSfCol0 = 2 * kAccCols;    // scale slot of stage s: kSfCol0 + 8 s (A: +0..3, B: +4..7)
 constexpr int kTmemCols = 512;
@@ -50,23 +53,12 @@ constexpr int kMaxGroups = 1024;
 constexpr int kTableBytes = (kMaxGroups + 8) * 4;
 constexpr int kBarBytes = 256;
 constexpr int kEpiBytes = 4 * 32 * 33 * 4;
-constexpr int kSfBytes = 1024;           // per stage: A block (512 B) + B block (512 B)
 constexpr int kSmem = 1024 + kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes +
                       kStages * kSfBytes;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kSfCol0 + 8 * kStages <= kTmemCols, "TMEM budget");
 static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
-
-// Four E8M0 scale bytes (K blocks 4kb .. 4kb+3) of one row; rows past the
-// matrix and blocks past the row read as 127 (2^0).
-__device__ __forceinline__ uint32_t scale_word(const uint8_t* s, int row, int rows, int stride, int kb) {
-  if (row >= rows) return 0x7F7F7F7Fu;
-  const uint8_t* p = s + (size_t)row * stride + 4 * kb;
-  if ((stride & 3) == 0) return __ldg(reinterpret_cast<const uint32_t*>(p));
-  uint32_t v = 0;
-  for (int b = 0; b < 4; ++b) v |= (uint32_t)((4 * kb + b < stride) ? __ldg(p + b) : 127) << (8 * b);
-  return v;
-}
+static_assert(kTableBytes % 16 == 0 && kEpiBytes % 16 == 0, "scale atoms need 16-byte alignment");
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -82,8 +74,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + kStages * kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + kTableBytes);
   float* epi_stage = reinterpret_cast<float*>(base + kStages * kStageBytes + kTableBytes + kBarBytes);
-  uint8_t* sf_smem = base + kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes;
-  const uint32_t sf_smem0 = smem_u32(sf_smem);
+  const uint32_t sf_smem0 =
+      stage0 + (uint32_t)(kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -102,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1 + 4);  // producer (with the TMA bytes) + 4 scale writers
+      mbar_init(full_bar(s), 1);  // the producer's arrival carries all the stage's bytes
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -148,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[p.G];
-  const int n_k = (p.num_kb + 1) / 2;  // p.num_kb counts 64-wide slices; a stage holds two
+  const int n_k = p.num_kb / 2;  // p.num_kb counts 64-wide slices; a stage holds two
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -162,6 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int act_row = ti.row0 + ti.tt * 128;
         const int w_row0 = ti.g * p.N + ti.wt * W_COLS;
         const int w_row1 = MODE == 0 ? w_row0 : w_row0 + 64;
+        // Atom row blocks: A by token tile, B by 128 rows of the weight atom
+        // matrix (GEMM-1: gate/up interleaved per 64 rows; GEMM-2: down).
+        const long long a_blk = tile_start[ti.g] / n_wt + ti.tt;
+        const long long b_blk = MODE == 0 ? (long long)ti.g * (2 * p.N / 128) + ti.wt
+                                          : (long long)ti.g * (p.N / 128) + ti.wt;
+        const uint8_t* a_atoms = p.s_act + a_blk * n_k * kAtomBytes;
+        const uint8_t* b_atoms = p.s_w0 + b_blk * n_k * kAtomBytes;
         for (int kb = 0; kb < n_k; ++kb) {
           if (!mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
                                  MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns)) {
@@ -169,12 +168,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = full_bar(rg.s);
-          mbar_arrive_expect_tx(fb, kStageBytes);
+          mbar_arrive_expect_tx(fb, kStageBytes + kSfBytes);
           const uint32_t st = stage0 + rg.s * kStageBytes;
+          const uint32_t sf = sf_smem0 + rg.s * kSfBytes;
           const int kx = kb * kK;
           tma_load_2d(st, &map_act, fb, kx, act_row);
           tma_load_2d_hint(st + kTileBytes, &map_w0, fb, kx, w_row0, pol);
           tma_load_2d_hint(st + kTileBytes + kTileBytes / 2, &map_w1, fb, kx, w_row1, pol);
+          bulk_load_hint(sf, a_atoms + (size_t)kb * kAtomBytes, kAtomBytes, fb, pol);
+          bulk_load_hint(sf + kAtomBytes, b_atoms + (size_t)kb * kAtomBytes, kAtomBytes, fb, pol);
           armed.mark(rg);
           rg.next(kStages);
         }
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = stage0 + rg.s * kStageBytes;
           const uint32_t sf = tmem_base + (uint32_t)(kSfCol0 + 8 * rg.s);
           tmem_cp_32x128b_warpx4(sf, sf_smem0 + rg.s * kSfBytes);
-          tmem_cp_32x128b_warpx4(sf + 4, sf_smem0 + rg.s * kSfBytes + 512);
+          tmem_cp_32x128b_warpx4(sf + 4, sf_smem0 + rg.s * kSfBytes + kAtomBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             umma_mxf8(d, sw128_kmajor_desc(st + k * 32), sw128_kmajor_desc(st + kTileBytes + k * 32),
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(drain_bar, 0, 100000000ull);
       }
     }
-  } else if (warp < kSfWarp0) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     float* stg = epi_stage + q * 32 * 33;
@@ -249,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rv = r < ti.nrows;
       if (MODE == 0) {
         // h = silu(gate) * up for columns 0..63 (gate) / 64..127 (up), MXFP8 per 32.
+        // Its scale bytes go to the atoms of this token tile (row q*32+lane).
+        const long long a_blk = tile_start[ti.g] / n_wt + ti.tt;
+        uint8_t* h_atoms = p.out_scale + a_blk * (p.N / 128) * kAtomBytes;
 #pragma unroll 1
         for (int c = 0; c < 64; c += 32) {
           uint32_t g[32], u[32];
@@ -281,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.N + col);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            p.out_scale[row * (p.N / 32) + col / 32] = (uint8_t)code;
+            h_atoms[(size_t)(col / 128) * kAtomBytes + atom_byte(q * 32 + lane, (col / 32) & 3)] =
+                (uint8_t)code;
           }
         }
       } else {
@@ -310,66 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
-  } else {
-    // ------------------------------------------------------------ scale writers
-    // Warp w (0..3 here) handles A row and B row 32w + lane: their scale
-    // words go to byte 16 lane + 4 w of the stage's A and B blocks.
-    const int q = warp - kSfWarp0;
-    auto load_words = [&](int tile, int kb, uint32_t& wa, uint32_t& wb) {
-      const TileInfo ti = decode_tile<128>(p, tile_start, tile);
-      const int m = q * 32 + lane;
-      const int act_row = ti.row0 + ti.tt * 128 + m;
-      wa = (ti.tt * 128 + m < ti.nrows) ? scale_word(p.s_act, act_row, p.rows, p.sstride, kb)
-                                         : 0x7F7F7F7Fu;
-      const int w_row0 = ti.g * p.N + ti.wt * W_COLS;
-      const int w_row1 = MODE == 0 ? w_row0 : w_row0 + 64;
-      wb = m < 64 ? scale_word(p.s_w0, w_row0 + m, p.w_rows, p.sstride, kb)
-                  : scale_word(p.s_w1, w_row1 + m - 64, p.w_rows, p.sstride, kb);
-    };
-    // Scale words are loaded kPre stages ahead into a small register ring.
-    constexpr int kPre = 4;
-    int cur_tile = blockIdx.x, cur_kb = 0, pre_tile = blockIdx.x, pre_kb = 0;
-    auto advance = [&](int& t, int& k) {
-      if (++k == n_k) {
-        k = 0;
-        t += gridDim.x;
-      }
-    };
-    uint32_t qa[kPre], qb[kPre];
-#pragma unroll
-    for (int i = 0; i < kPre; ++i) {
-      qa[i] = 0x7F7F7F7Fu;
-      qb[i] = 0x7F7F7F7Fu;
-      if (pre_tile < total) load_words(pre_tile, pre_kb, qa[i], qb[i]);
-      advance(pre_tile, pre_kb);
-    }
-    Ring rg;
-    bool ok = true;
-    while (ok && cur_tile < total) {
-#pragma unroll
-      for (int i = 0; i < kPre; ++i) {
-        if (!ok || cur_tile >= total) break;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
-                                  MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        uint32_t* blk = reinterpret_cast<uint32_t*>(sf_smem + rg.s * kSfBytes);
-        blk[lane * 4 + q] = qa[i];
-        blk[128 + lane * 4 + q] = qb[i];
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(rg.s));
-        rg.next(kStages);
-        if (pre_tile < total) load_words(pre_tile, pre_kb, qa[i], qb[i]);
-        advance(pre_tile, pre_kb);
-        advance(cur_tile, cur_kb);
-      }
-    }
   }
 
   tc_fence_before();
@@ -390,6 +336,8 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   const void* w0 = MODE == 0 ? a.w_gate : a.w_down;
   const void* w1 = MODE == 0 ? a.w_up : a.w_down;
   if (a.rows == 0 || a.G == 0) return cudaSuccess;
+  // Whole atoms along K and along the weight rows of a tile.
+  if (a.H % 128 || a.I % 128 || a.G > kMaxGroups) return cudaErrorInvalidValue;
   const int G = a.offsets ? a.G : 1;
   CUtensorMap m_act, m_w0, m_w1;
   if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) ||
@@ -400,16 +348,13 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   p.offsets = a.offsets;
   p.G = G;
   p.rows = a.rows;
-  p.num_kb = (Kdim + 63) / 64;
+  p.num_kb = Kdim / 64;
   p.N = N;
   p.out = MODE == 0 ? a.h : static_cast<void*>(a.y);
   p.status = a.status;
   p.limit_ns = a.wait_limit_ns;
-  p.s_w0 = MODE == 0 ? a.s_gate : a.s_down;
-  p.s_w1 = MODE == 0 ? a.s_up : a.s_down;
-  p.sstride = Kdim / 32;
-  p.w_rows = G * N;
-  p.s_act = act_scale;
+  p.s_w0 = MODE == 0 ? a.s_gate : a.s_down;  // weight scale atoms
+  p.s_act = act_scale;                       // activation scale atoms, by token tile
   p.out_scale = MODE == 0 ? a.h_scale : nullptr;
   constexpr int W_COLS = MODE == 0 ? 64 : 128;
   const long long n_wt = (N + W_COLS - 1) / W_COLS;

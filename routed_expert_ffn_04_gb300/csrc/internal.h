@@ -55,9 +55,12 @@ struct GroupedGemmArgs {
   int route_norm;
   int mode;                // GemmMode
   int mx;                  // 1: weights are E4M3 + E8M0/32 (h MX-rounded too)
-  const uint8_t* a_scale;  // native MXFP8: E8M0 scales of `a` [rows, H/32] (a holds E4M3 codes)
-  uint8_t* h_scale;        // native MXFP8: E8M0 scales of h [rows, I/32] (h holds E4M3 codes)
-  const uint8_t* s_gate;   // MX scales [G*I, H/32], [G*I, H/32], [G*H, I/32]
+  // Native MXFP8 (gemm_mx.cu): a / h hold E4M3 codes, their scales are atoms
+  // by token tile of each group; s_gate the gate/up atoms, s_down the down atoms.
+  // The WQ converter path of gemm.cu reads s_gate, s_up, s_down row-major.
+  const uint8_t* a_scale;
+  uint8_t* h_scale;
+  const uint8_t* s_gate;
   const uint8_t* s_up;
   const uint8_t* s_down;
   int num_sms;
@@ -88,9 +91,27 @@ cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32
                            cudaStream_t s);
 
 // ---- MX quantiser (mxquant.cu)
-// q / scale / deq may each be null; deq receives the dequantised values as bf16.
+// q / scale / atoms / deq may each be null. scale: row-major [rows, cols/32];
+// atoms: the scale atoms of the rows as one group (cols % 128 == 0; the rows
+// of the last 128-row block past `rows` are left untouched); deq: the
+// dequantised values as bf16.
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, void* deq, cudaStream_t s);
+                               uint8_t* scale, uint8_t* atoms, void* deq, cudaStream_t s);
+
+// ---- scale atoms (mxpack.cu; layout in mx_layout.cuh)
+// Row-major E8M0 scales [rows, cols/32] -> atoms. s1 == nullptr: the atoms
+// of s0 (rows % 128 == 0). Else gate (s0) and up (s1) interleaved per 64 rows
+// (rows % 64 == 0), 2 * rows atom-matrix rows. cols % 128 == 0.
+cudaError_t launch_pack_weight_scales(const uint8_t* s0, const uint8_t* s1, int64_t rows, int cols,
+                                      uint8_t* out, cudaStream_t s);
+// Activation scales [src_rows, cols/32] -> atoms by token tile of each group
+// (offsets [G+1], or nullptr for one group of `rows`). Row j of group g takes
+// the scales of src row perm_src[offsets[g] + j] / K (nullptr: offsets[g] + j).
+cudaError_t launch_gather_scale_atoms(const uint8_t* src, int src_rows, int cols,
+                                      const int32_t* perm_src, int K, const int32_t* offsets,
+                                      int G, int rows, uint8_t* out, int* status, cudaStream_t s);
+// Bytes of activation atoms for `rows` rows in at most `groups` groups.
+size_t scale_atom_bytes(int64_t rows, int groups, int cols);
 // out[r, c] = bf16(e4m3(q[r, c]) * 2^(scale[r, c/32] - 127)).
 cudaError_t launch_mx_dequantize(const uint8_t* q, const uint8_t* scale, int64_t rows, int cols,
                                  void* out_bf16, cudaStream_t s);

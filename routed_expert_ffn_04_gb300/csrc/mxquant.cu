@@ -7,7 +7,8 @@
 //   scale code = clamp(shared_exp, -127, 127) + 127;  amax == 0 -> code 0
 //   element    = RNE(v / 2^shared_exp) to E4M3, saturating at +-448
 // One thread per block of 32: 64 bytes in (four 16-byte loads), 32 code
-// bytes out (two 16-byte stores) and one scale byte; optionally the
+// bytes out (two 16-byte stores) and one scale byte, row-major and/or in the
+// scale atoms of the block-scaled GEMM (mx_layout.cuh); optionally the
 // dequantised block as bf16 (exact: an E4M3 value times a power of two).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -15,6 +16,7 @@
 
 #include "internal.h"
 #include "mx.cuh"
+#include "mx_layout.cuh"
 
 namespace moe {
 namespace {
@@ -23,6 +25,7 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
                                                        long long nblocks,
                                                        uint4* __restrict__ q,
                                                        uint8_t* __restrict__ scale,
+                                                       uint8_t* __restrict__ atoms, int nb,
                                                        uint4* __restrict__ deq) {
   const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nblocks) return;
@@ -54,6 +57,12 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
     }
   }
   if (scale) scale[b] = (uint8_t)code;
+  if (atoms) {  // nb = blocks per row, a multiple of 4
+    const long long row = b / nb;
+    const int blk = (int)(b - row * nb);
+    atoms[((row >> 7) * (nb >> 2) + (blk >> 2)) * kAtomBytes + atom_byte((int)(row & 127), blk & 3)] =
+        (uint8_t)code;
+  }
   if (q) {
     q[b * 2] = make_uint4(words[0], words[1], words[2], words[3]);
     q[b * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
@@ -86,13 +95,14 @@ __global__ void __launch_bounds__(256) mx_dequant_kernel(const uint4* __restrict
 }  // namespace
 
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, void* deq, cudaStream_t s) {
+                               uint8_t* scale, uint8_t* atoms, void* deq, cudaStream_t s) {
   const long long nblocks = (long long)rows * (cols / 32);
   if (nblocks == 0) return cudaSuccess;
+  if (atoms && cols % 128) return cudaErrorInvalidValue;
   const long long grid = (nblocks + 255) / 256;
   mx_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
-                                                 reinterpret_cast<uint4*>(q), scale,
-                                                 static_cast<uint4*>(deq));
+                                                 reinterpret_cast<uint4*>(q), scale, atoms,
+                                                 cols / 32, static_cast<uint4*>(deq));
   return cudaGetLastError();
 }
 

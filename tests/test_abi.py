@@ -39,7 +39,30 @@ def test_workspace_size_covers_the_buffers(lib):
     assert n >= TK * H * 2 + TK * I * 2 + TK * H * 4 + T * H * 4
     assert moe.workspace_size(_cfg(T=128)) > n
     assert moe.grouped_gemm_workspace_size(512, 4096, 1536) >= 512 * 1536 * 2
-    assert moe.grouped_gemm_workspace_size(512, 4096, 1536, moe.MOE_MXFP8_E4M3) >= 512 * 1536 + 512 * 1536 // 32
+    # MXFP8: h codes, plus scale atoms of h and of a with one 128-row block of slack per group.
+    mx1 = moe.grouped_gemm_workspace_size(512, 4096, 1536, moe.MOE_MXFP8_E4M3)
+    assert mx1 >= 512 * 1536 + (512 // 128 + 1) * (1536 + 4096) // 32 * 128
+    mx8 = moe.grouped_gemm_workspace_size(512, 4096, 1536, moe.MOE_MXFP8_E4M3, num_groups=8)
+    assert mx8 - mx1 >= 7 * (1536 + 4096) // 32 * 128
+
+
+def test_mx_config_needs_whole_scale_atoms(lib):
+    n = ctypes.c_size_t(0)
+    for bad in (dict(H=4032), dict(I=1472), dict(I_shared=64)):
+        c = _cfg(dtype=moe.MOE_MXFP8_E4M3, **bad)
+        assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_size(ctypes.byref(_cfg(dtype=moe.MOE_MXFP8_E4M3)), ctypes.byref(n)) == moe.MOE_OK
+
+
+def test_pack_mx_scales_argument_checks(lib):
+    P = ctypes.c_void_p
+    # cols not a multiple of 128, rows not a multiple of 128 (single) or 64 (pair), misaligned pointer.
+    assert lib.moe_pack_mx_scales(None, P(256), None, 128, 96, P(256), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_mx_scales(None, P(256), None, 64, 128, P(256), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_mx_scales(None, P(256), P(512), 96, 128, P(256), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_mx_scales(None, P(260), None, 128, 128, P(256), None) == moe.MOE_ERR_INVALID_ARG
+    # Valid sizes with a null handle: rejected as an argument, before any launch.
+    assert lib.moe_pack_mx_scales(None, P(256), P(512), 64, 128, P(256), None) == moe.MOE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("bad", [dict(K=0), dict(K=9, E=8), dict(E=2048, K=8), dict(H=100), dict(I=96),

@@ -100,8 +100,31 @@ def _mx_weights_oracle(w):
     return {k: oracle.mx_quantize(v.cpu()) for k, v in w.items()}
 
 
+def _atom_matrix(atoms, cols):
+    """Inverse of the scale-atom layout (moe_pack_mx_scales in moe.h): row r of
+    128-row block b, K-block j of atom (b, a) at byte 512 (b * cols/128 + a)
+    + 16 (r % 32) + 4 (r / 32) + j. Returns the [rows, cols/32] matrix."""
+    nk = cols // 128
+    a = np.asarray(atoms, np.uint8).reshape(-1, nk, 32, 4, 4)   # [block, atom, r%32, r/32, j]
+    a = a.transpose(0, 3, 2, 1, 4)                               # [block, r/32, r%32, atom, j]
+    return a.reshape(-1, nk * 4)
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 512), (64 * 24, 4096)])
+def test_pack_mx_scales_bit_exact(handle, rows, cols):
+    g = torch.Generator().manual_seed(rows + cols)
+    s0 = torch.randint(0, 255, (rows, cols // 32), generator=g, dtype=torch.uint8)
+    s1 = torch.randint(0, 255, (rows, cols // 32), generator=g, dtype=torch.uint8)
+    if rows % 128 == 0:
+        got = _atom_matrix(moe.pack_mx_scales(handle, s0.cuda()).cpu().numpy(), cols)
+        assert np.array_equal(got, s0.numpy())
+    pair = _atom_matrix(moe.pack_mx_scales(handle, s0.cuda(), s1.cuda()).cpu().numpy(), cols)
+    want = np.stack([s0.numpy().reshape(-1, 64, cols // 32), s1.numpy().reshape(-1, 64, cols // 32)], 1)
+    assert np.array_equal(pair, want.reshape(2 * rows, cols // 32))
+
+
 @pytest.mark.parametrize("mode", [1, 2])
-@pytest.mark.parametrize("H,I,sizes", [(256, 128, [16, 0, 3, 1]), (512, 320, [0, 1, 37, 130, 300, 0])])
+@pytest.mark.parametrize("H,I,sizes", [(256, 128, [16, 0, 3, 1]), (512, 384, [0, 1, 37, 130, 300, 0])])
 def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
@@ -111,12 +134,14 @@ def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
     wg, wu, wd = ((torch.randn(*sh, generator=g) * 0.02).to(torch.bfloat16) for sh in ((G, I, H), (G, I, H), (G, H, I)))
     aq, as_ = moe.quantize_mx(handle, a.cuda())
     mw = moe.quantize_weights_mx(handle, {"w_gate": wg.cuda(), "w_up": wu.cuda(), "w_down": wd.cuda()})
+    pw = moe.pack_weights_mx(handle, mw)
     handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
     y = torch.full((rows, H), float("nan"), dtype=torch.float32, device="cuda")
-    ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I, moe.MOE_MXFP8_E4M3), dtype=torch.uint8, device="cuda")
-    moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), mw["w_gate"], mw["w_up"], mw["w_down"], y, ws,
-                            num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP8_E4M3, a_scale=as_, s_gate=mw["s_gate"],
-                            s_up=mw["s_up"], s_down=mw["s_down"])
+    ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I, moe.MOE_MXFP8_E4M3, num_groups=G), dtype=torch.uint8,
+                     device="cuda")
+    moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), pw["w_gate"], pw["w_up"], pw["w_down"], y, ws,
+                            num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP8_E4M3, a_scale=as_, s_gate=pw["s_gate"],
+                            s_down=pw["s_down"])
     torch.cuda.synchronize()
     assert handle.device_status() == 0
     yh = y.cpu().numpy()
@@ -152,7 +177,7 @@ def test_mx_layer_tiny(handle, mode):
 
 @pytest.mark.parametrize("mode", [1, 2])
 def test_mx_layer_ragged_shape(handle, mode):
-    shape = synth.MoEShape("mxr", T=45, H=384, E=13, K=3, I=192, I_shared=128, dtype="mxfp8")
+    shape = synth.MoEShape("mxr", T=45, H=384, E=13, K=3, I=256, I_shared=128, dtype="mxfp8")
     x, logits = synth.make_activations(shape, seed=5)
     w = synth.make_weights(shape, seed=5)
     out = _run_mx_layer(handle, shape, x.cuda(), logits.cuda(), {k: v.cuda() for k, v in w.items()}, mode)
