@@ -11,7 +11,7 @@ Prints ONE JSON line (rank 0). Multi-GPU (torchrun): every rank runs its own
 replica on its own tokens (no collective on the data path); `value` is the
 tokens of all ranks divided by the slowest rank's time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|mxfp8|tiny]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 """
 from __future__ import annotations
@@ -167,13 +167,16 @@ def algorithmic_work(shape, counts):
     """Bytes the layer must move and FLOPs it must do, from the expert counts."""
     H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
     touched = int((counts > 0).sum())
-    wb = 1 + 1 / 32 if shape.dtype == "mxfp8" else 2  # bytes per weight element (E4M3 + E8M0/32, or bf16)
+    # Bytes per GEMM operand element: bf16, or MXFP8's E4M3 code plus its share
+    # of the E8M0 scale (one per 32). x, logits and out are bf16 / fp32 either way.
+    wb = 1 + 1 / 32 if shape.dtype == "mxfp8" else 2
     w_expert = 3 * H * I * wb
     w_shared = 3 * H * Is * wb
     layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2)
     flops = 6 * H * I * T * K + 6 * H * Is * T
     TK = T * K
-    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * 2 + TK * I * 2)
+    # GEMM-1 reads the touched experts' gate/up weights and x_perm, and writes h.
+    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * wb + TK * I * wb)
     return dict(touched=touched, layer_bytes=layer_bytes, flops=flops, gemm1_bytes=gemm1_bytes,
                 gemm1_flops=4 * H * I * TK)
 
@@ -302,7 +305,9 @@ def run_ours(args):
         traffic = int(GEMM1_TRAFFIC["bytes_per_touched_expert"] * work["touched"])
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
-    launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1
+    # route 1, permute 3 + row gather 1, GEMMs 2, shared GEMMs 2, combine 1;
+    # MXFP8 adds the quantiser of x and the gather of its scale atoms.
+    launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1 + (2 if shape.dtype == "mxfp8" else 0)
 
     result = {
         "metric": METRIC,
@@ -315,8 +320,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8 (E4M3 weights + E8M0/32; bf16 tensor-core inputs, fp32 accumulate)"
-                 if shape.dtype == "mxfp8" else "bf16",
+        "dtype": "mxfp8 (E4M3 activations and weights, E8M0 scale per 32 along K, block-scaled tensor "
+                 "cores, fp32 accumulate)" if shape.dtype == "mxfp8" else "bf16",
         "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
         "config": {
             "workload": (f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer")
