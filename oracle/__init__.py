@@ -8,10 +8,11 @@ never calls it, and the two share no code.
 Sources (page titles):
   [Hy3]  "腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战", section 一
          (model facts), section 8.5 (shared-expert multi-stream), section 8.2
-         (MXFP8 W8A8).
+         (MXFP8 W8A8; MXFP4 routed experts with MXFP8 activations, W4A8).
   [HyI3] "HunyuanImage-3.0 MoE 多流变体实战", 源码级实现拆解 §3 (output =
          hidden_states_mlp + combined_output).
-  [OCP-MX] OCP Microscaling Formats (MX) v1.0, conversion to MX formats.
+  [OCP-MX] OCP Microscaling Formats (MX) v1.0, conversion to MX formats and
+         the E4M3 / E2M1 element-format tables.
 
 Parity is pinned for every function here by the ``-m "not gpu"`` tests
 (brute force, closed forms, invariants, library routines).
@@ -56,8 +57,14 @@ def _load():
             lib.oracle_permute.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_swiglu_mlp.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_layer_forward.argtypes = [i, i, i, i, i, i, d, i] + [P] * 8 + [i, P, P, P, P]
-            lib.oracle_layer_forward_mx.argtypes = [i, i, i, i, i, i, d, i] + [P] * 14 + [i, P, P]
-            lib.oracle_swiglu_mlp_mx.argtypes = [i, i, i] + [P] * 9
+            lib.oracle_layer_forward_mx.argtypes = [i, i, i, i, i, i, i, d, i] + [P] * 14 + [i, P, P]
+            lib.oracle_swiglu_mlp_mx.argtypes = [i, i, i, i] + [P] * 9
+            lib.oracle_mxfp4_quantize_bf16.argtypes = [i, i, P, P, P]
+            lib.oracle_mxfp4_dequantize.argtypes = [i, i, P, P, P]
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_value.restype = d
+            lib.oracle_e2m1_encode.argtypes = [d]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
             lib.oracle_mx_quantize_bf16.argtypes = [i, i, P, P, P]
             lib.oracle_mx_quantize_f64.argtypes = [i, i, P, P, P]
             lib.oracle_mx_dequantize.argtypes = [i, i, P, P, P]
@@ -204,6 +211,39 @@ def mx_quantize(a) -> tuple[np.ndarray, np.ndarray]:
     return q.reshape(lead + (cols,)), s.reshape(lead + (cols // 32,))
 
 
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def mxfp4_quantize(a) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4 quantisation along the last axis ([OCP-MX] rule, E2M1 elements) of a bf16 tensor.
+
+    Returns (packed codes uint8 [..., cols/2], element 2j in the low nibble;
+    scales uint8 [..., cols/32]).
+    """
+    a2 = _bf16_bits(a)
+    a2 = np.ascontiguousarray(a2.reshape(-1, a2.shape[-1]))
+    rows, cols = a2.shape
+    q = np.empty((rows, cols // 2), np.uint8)
+    s = np.empty((rows, cols // 32), np.uint8)
+    _check(_load().oracle_mxfp4_quantize_bf16(rows, cols, _ptr(a2), _ptr(q), _ptr(s)), "mxfp4_quantize")
+    lead = tuple(a.shape[:-1])
+    return q.reshape(lead + (cols // 2,)), s.reshape(lead + (cols // 32,))
+
+
+def mxfp4_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    q2 = np.ascontiguousarray(q.reshape(-1, q.shape[-1]), dtype=np.uint8)
+    s2 = np.ascontiguousarray(s.reshape(-1, s.shape[-1]), dtype=np.uint8)
+    rows, cols = q2.shape[0], q2.shape[1] * 2
+    out = np.empty((rows, cols), np.float64)
+    _check(_load().oracle_mxfp4_dequantize(rows, cols, _ptr(q2), _ptr(s2), _ptr(out)), "mxfp4_dequantize")
+    return out.reshape(q.shape[:-1] + (cols,))
+
+
 def mx_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     q2 = np.ascontiguousarray(q.reshape(-1, q.shape[-1]), dtype=np.uint8)
     s2 = np.ascontiguousarray(s.reshape(-1, s.shape[-1]), dtype=np.uint8)
@@ -213,17 +253,19 @@ def mx_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return out.reshape(q.shape)
 
 
-def layer_forward_mx(x, logits, mx_w, *, K: int, scaling: float, route_norm: bool = True, tokens=None):
-    """The whole layer in MXFP8 mode (float64 out) for `tokens`.
+def layer_forward_mx(x, logits, mx_w, *, K: int, scaling: float, route_norm: bool = True, tokens=None,
+                     w4: bool = False):
+    """The whole layer in MX mode (float64 out) for `tokens`.
 
     mx_w: dict with 'w_gate','w_up','w_down','ws_gate','ws_up','ws_down', each a
-    (codes, scales) pair as returned by mx_quantize.
+    (codes, scales) pair as returned by mx_quantize; with w4 (W4A8) the routed
+    'w_*' pairs come from mxfp4_quantize instead (packed E2M1 codes).
     """
     x = _bf16_bits(x)
     logits = np.ascontiguousarray(np.asarray(logits.cpu() if hasattr(logits, "cpu") else logits), dtype=np.float32)
     T, H = x.shape
     qg, sg = mx_w["w_gate"]
-    E, I, _ = qg.shape
+    E, I = qg.shape[0], qg.shape[1]
     qs = mx_w["ws_gate"][0]
     Is = qs.shape[0]
     arrs = []
@@ -233,25 +275,27 @@ def layer_forward_mx(x, logits, mx_w, *, K: int, scaling: float, route_norm: boo
     tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
     n = tokens.shape[0]
     out = np.empty((n, H), np.float64)
-    _check(_load().oracle_layer_forward_mx(T, H, E, K, I, Is, float(scaling), int(route_norm), _ptr(x), _ptr(logits),
+    _check(_load().oracle_layer_forward_mx(int(w4), T, H, E, K, I, Is, float(scaling), int(route_norm), _ptr(x),
+                                           _ptr(logits),
                                            *[_ptr(a) for a in arrs], n, _ptr(tokens), _ptr(out)), "layer_forward_mx")
     return out
 
 
-def swiglu_mlp_mx(xq: np.ndarray, xs: np.ndarray, w_gate, w_up, w_down) -> np.ndarray:
+def swiglu_mlp_mx(xq: np.ndarray, xs: np.ndarray, w_gate, w_up, w_down, w4: bool = False) -> np.ndarray:
     """Dense SwiGLU MLP on MX-quantised rows with MX weights ([Hy3] section 8.2).
 
     xq/xs: codes [R, H] and scales [R, H/32]; w_*: (codes, scales) pairs with
-    w_gate/w_up codes [I, H] and w_down codes [H, I]. Returns float64 [R, H].
+    w_gate/w_up codes [I, H] and w_down codes [H, I] (w4: packed E2M1 codes
+    [I, H/2] and [H, I/2] from mxfp4_quantize). Returns float64 [R, H].
     """
     xq = np.ascontiguousarray(xq, dtype=np.uint8)
     xs = np.ascontiguousarray(xs, dtype=np.uint8)
     R, H = xq.shape
-    I = w_gate[0].shape[0]
+    I = w_gate[1].shape[0]
     arrs = []
     for q, sc in (w_gate, w_up, w_down):
         arrs += [np.ascontiguousarray(q, dtype=np.uint8), np.ascontiguousarray(sc, dtype=np.uint8)]
     y = np.empty((R, H), np.float64)
-    _check(_load().oracle_swiglu_mlp_mx(R, H, I, _ptr(xq), _ptr(xs), *[_ptr(a) for a in arrs], _ptr(y)),
+    _check(_load().oracle_swiglu_mlp_mx(int(w4), R, H, I, _ptr(xq), _ptr(xs), *[_ptr(a) for a in arrs], _ptr(y)),
            "swiglu_mlp_mx")
     return y

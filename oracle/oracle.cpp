@@ -399,16 +399,107 @@ int oracle_mx_dequantize(int rows, int cols, const uint8_t* q, const uint8_t* sc
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// MXFP4 (E2M1 elements, one E8M0 scale per 32): the routed-expert weights of
+// the W4A8 recipe ([Hy3] section 8.2: MXFP4 routed experts with MXFP8
+// activations; the shared expert stays W8A8). Same [OCP-MX] conversion rule
+// with emax_elem = 2 for E2M1:
+//   shared_exp = floor(log2(amax)) - 2; X = 2^shared_exp (E8M0);
+//   P_i = v_i / X rounded to nearest-even E2M1, saturating to +-6.
+// Two codes per byte: element 2j in the low nibble, 2j+1 in the high nibble.
+// ---------------------------------------------------------------------------
+
+// Value of an E2M1 code (low 4 bits) from the format definition: 1 sign bit,
+// 2 exponent bits (bias 1), 1 mantissa bit; no infinities or NaN.
+double oracle_e2m1_value(uint8_t code) {
+  const int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = (e == 0) ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+// Nearest E2M1 magnitude code 0..7 to a >= 0, ties to the even mantissa;
+// values past 6 saturate.
+static uint8_t e2m1_round_magnitude(double a) {
+  if (a >= oracle_e2m1_value(7)) return 7;
+  int lo = 0, hi = 7;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (oracle_e2m1_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
+  }
+  const double dlo = a - oracle_e2m1_value((uint8_t)lo), dhi = oracle_e2m1_value((uint8_t)hi) - a;
+  if (dlo < dhi) return (uint8_t)lo;
+  if (dhi < dlo) return (uint8_t)hi;
+  return (lo & 1) ? (uint8_t)hi : (uint8_t)lo;
+}
+
+// Sign-magnitude E2M1 code; a magnitude that rounds to zero keeps the sign.
+uint8_t oracle_e2m1_encode(double v) {
+  const uint8_t mag = e2m1_round_magnitude(std::fabs(v));
+  return std::signbit(v) ? (uint8_t)(mag | 8) : mag;
+}
+
+// One block of n values (n <= 32, even) -> n/2 packed bytes + one scale.
+static void mxfp4_block(const double* v, int n, uint8_t* q, uint8_t* scale) {
+  double amax = 0.0;
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(v[i]));
+  for (int i = 0; i < n / 2; ++i) q[i] = 0;
+  if (amax == 0.0) {
+    *scale = 0;
+    return;
+  }
+  int ex;
+  std::frexp(amax, &ex);           // amax = f * 2^ex, f in [0.5, 1)
+  int shared_exp = (ex - 1) - 2;   // floor(log2(amax)) - emax_elem(E2M1)
+  if (shared_exp < -127) shared_exp = -127;
+  if (shared_exp > 127) shared_exp = 127;
+  *scale = (uint8_t)(shared_exp + 127);
+  const double X = std::ldexp(1.0, shared_exp);
+  for (int i = 0; i < n; ++i) q[i / 2] |= (uint8_t)(oracle_e2m1_encode(v[i] / X) << (4 * (i & 1)));
+}
+
+// Quantise a [rows, cols] bf16 matrix along cols: q [rows, cols/2] packed
+// E2M1 codes, scale [rows, cols/32] E8M0 codes.
+int oracle_mxfp4_quantize_bf16(int rows, int cols, const uint16_t* in, uint8_t* q,
+                               uint8_t* scale) {
+  if (rows < 0 || cols <= 0 || cols % 32) return -1;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    double v[32];
+    for (int b = 0; b < cols / 32; ++b) {
+      for (int i = 0; i < 32; ++i) v[i] = bf16_to_double(in[(size_t)r * cols + b * 32 + i]);
+      mxfp4_block(v, 32, q + (size_t)r * (cols / 2) + b * 16, scale + (size_t)r * (cols / 32) + b);
+    }
+  }
+  return 0;
+}
+
+// Dequantise: value = 2^(scale-127) * e2m1_value(code).
+int oracle_mxfp4_dequantize(int rows, int cols, const uint8_t* q, const uint8_t* scale,
+                            double* out) {
+  if (rows < 0 || cols <= 0 || cols % 32) return -1;
+  for (int r = 0; r < rows; ++r)
+    for (int c = 0; c < cols; ++c) {
+      const double X = std::ldexp(1.0, (int)scale[(size_t)r * (cols / 32) + c / 32] - 127);
+      const uint8_t byte = q[(size_t)r * (cols / 2) + c / 2];
+      out[(size_t)r * cols + c] = X * oracle_e2m1_value((c & 1) ? byte >> 4 : byte & 15);
+    }
+  return 0;
+}
+
 // One expert SwiGLU FFN row on MX operands: x is already dequantised (double);
 // weights are MX codes + scales; h is MX-quantised (dynamic, per 32 along I)
 // before the down projection, as the MXFP8 activation path quantises every
 // Linear input ([Hy3] section 8.2: routed and shared Linears in W8A8 MXFP8).
-static double mx_weight(const uint8_t* q, const uint8_t* s, int cols, size_t r, int c) {
-  return std::ldexp(1.0, (int)s[r * (cols / 32) + c / 32] - 127) *
-         oracle_e4m3_value(q[r * cols + c]);
+// Weight format wfmt: 0 = E4M3 codes (one per byte), 1 = E2M1 codes (two per
+// byte, [rows, cols/2]).
+static double mx_weight(int wfmt, const uint8_t* q, const uint8_t* s, int cols, size_t r, int c) {
+  const double X = std::ldexp(1.0, (int)s[r * (cols / 32) + c / 32] - 127);
+  if (wfmt == 0) return X * oracle_e4m3_value(q[r * cols + c]);
+  const uint8_t byte = q[r * (cols / 2) + c / 2];
+  return X * oracle_e2m1_value((c & 1) ? byte >> 4 : byte & 15);
 }
 
-static void swiglu_row_mx(int H, int I, const double* x, const uint8_t* qg,
+static void swiglu_row_mx(int wfmt, int H, int I, const double* x, const uint8_t* qg,
                           const uint8_t* sg, const uint8_t* qu, const uint8_t* su,
                           const uint8_t* qd, const uint8_t* sd, double* y) {
   std::vector<double> h(I), hd(I);
@@ -416,8 +507,8 @@ static void swiglu_row_mx(int H, int I, const double* x, const uint8_t* qg,
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int c = 0; c < H; ++c) {
-      g += mx_weight(qg, sg, H, i, c) * x[c];
-      u += mx_weight(qu, su, H, i, c) * x[c];
+      g += mx_weight(wfmt, qg, sg, H, i, c) * x[c];
+      u += mx_weight(wfmt, qu, su, H, i, c) * x[c];
     }
     h[i] = silu(g) * u;
   }
@@ -425,34 +516,35 @@ static void swiglu_row_mx(int H, int I, const double* x, const uint8_t* qg,
   oracle_mx_dequantize(1, I, hq.data(), hs.data(), hd.data());
   for (int m = 0; m < H; ++m) {
     double acc = 0.0;
-    for (int i = 0; i < I; ++i) acc += mx_weight(qd, sd, I, m, i) * hd[i];
+    for (int i = 0; i < I; ++i) acc += mx_weight(wfmt, qd, sd, I, m, i) * hd[i];
     y[m] = acc;
   }
 }
 
 // Dense SwiGLU MLP over rows whose activations are already MX-quantised
-// (xq codes [R, H], xs scales [R, H/32]) with MX weights: dequantise x, then
-// the same row function as the MXFP8 layer (h re-quantised per 32 along I).
-// [Hy3] section 8.2: routed and shared Linears in W8A8 MXFP8.
-int oracle_swiglu_mlp_mx(int R, int H, int I, const uint8_t* xq, const uint8_t* xs,
+// (xq codes [R, H], xs scales [R, H/32]) with MX weights (format wfmt, as in
+// mx_weight): dequantise x, then the same row function as the MX layer (h
+// re-quantised to MXFP8 per 32 along I). [Hy3] section 8.2.
+int oracle_swiglu_mlp_mx(int wfmt, int R, int H, int I, const uint8_t* xq, const uint8_t* xs,
                          const uint8_t* qg, const uint8_t* sg, const uint8_t* qu,
                          const uint8_t* su, const uint8_t* qd, const uint8_t* sd, double* y) {
-  if (R < 0 || H <= 0 || H % 32 || I <= 0 || I % 32) return -1;
+  if (R < 0 || H <= 0 || H % 32 || I <= 0 || I % 32 || wfmt < 0 || wfmt > 1) return -1;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < R; ++r) {
     std::vector<double> xd(H);
     oracle_mx_dequantize(1, H, xq + (size_t)r * H, xs + (size_t)r * (H / 32), xd.data());
-    swiglu_row_mx(H, I, xd.data(), qg, sg, qu, su, qd, sd, y + (size_t)r * H);
+    swiglu_row_mx(wfmt, H, I, xd.data(), qg, sg, qu, su, qd, sd, y + (size_t)r * H);
   }
   return 0;
 }
 
-// The whole layer in MXFP8 mode for a subset of tokens. x is given as bf16 and
+// The whole layer in MX mode for a subset of tokens. x is given as bf16 and
 // is MX-quantised here (dynamic activation quantisation); weights are given as
-// MX codes/scales (produced by oracle_mx_quantize_bf16 from the bf16 weights).
-// Routing, permutation, finalize and the shared add are as in
-// oracle_layer_forward.
-int oracle_layer_forward_mx(int T, int H, int E, int K, int I, int I_shared,
+// MX codes/scales (produced by oracle_mx_quantize_bf16 from the bf16 weights,
+// or for W4A8's routed experts (wfmt 1) by oracle_mxfp4_quantize_bf16; the
+// shared expert is always E4M3). Routing, permutation, finalize and the shared
+// add are as in oracle_layer_forward.
+int oracle_layer_forward_mx(int wfmt, int T, int H, int E, int K, int I, int I_shared,
                             double scaling, int route_norm, const uint16_t* x,
                             const float* logits, const uint8_t* qg, const uint8_t* sg,
                             const uint8_t* qu, const uint8_t* su, const uint8_t* qd,
@@ -461,7 +553,7 @@ int oracle_layer_forward_mx(int T, int H, int E, int K, int I, int I_shared,
                             const uint8_t* ssd, int n_sel, const int32_t* tokens,
                             double* out) {
   if (T <= 0 || H <= 0 || H % 32 || E <= 0 || K <= 0 || K > E || I <= 0 || I % 32 ||
-      I_shared < 0 || I_shared % 32 || n_sel < 0)
+      I_shared < 0 || I_shared % 32 || n_sel < 0 || wfmt < 0 || wfmt > 1)
     return -1;
   for (int j = 0; j < n_sel; ++j)
     if (tokens[j] < 0 || tokens[j] >= T) return -1;
@@ -495,15 +587,15 @@ int oracle_layer_forward_mx(int T, int H, int E, int K, int I, int I_shared,
   for (int r = 0; r < RK; ++r) {
     const int e = row_expert[r];
     const int j = perm_src[r] / K;
-    const size_t eIH = (size_t)e * I * H;
-    swiglu_row_mx(H, I, &xd[(size_t)j * H], qg + eIH, sg + eIH / 32, qu + eIH, su + eIH / 32,
-                  qd + eIH, sd + eIH / 32, &y_perm[(size_t)r * H]);
+    const size_t eIH = (size_t)e * I * H, eq = wfmt ? eIH / 2 : eIH;  // code bytes per expert
+    swiglu_row_mx(wfmt, H, I, &xd[(size_t)j * H], qg + eq, sg + eIH / 32, qu + eq, su + eIH / 32,
+                  qd + eq, sd + eIH / 32, &y_perm[(size_t)r * H]);
   }
   std::vector<double> s((size_t)n_sel * H, 0.0);
   if (I_shared > 0) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int j = 0; j < n_sel; ++j)
-      swiglu_row_mx(H, I_shared, &xd[(size_t)j * H], qsg, ssg, qsu, ssu, qsd, ssd,
+      swiglu_row_mx(0, H, I_shared, &xd[(size_t)j * H], qsg, ssg, qsu, ssu, qsd, ssd,
                     &s[(size_t)j * H]);
   }
   for (int j = 0; j < n_sel; ++j)
