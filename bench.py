@@ -11,7 +11,7 @@ Prints ONE JSON line (rank 0). Multi-GPU (torchrun): every rank runs its own
 replica on its own tokens (no collective on the data path); `value` is the
 tokens of all ranks divided by the slowest rank's time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|mxfp8|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|skewed|mxfp8|mxfp4|tiny]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 """
 from __future__ import annotations
@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8"])
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8", "mxfp4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--experts", type=int, default=None,
@@ -167,16 +167,20 @@ def algorithmic_work(shape, counts):
     """Bytes the layer must move and FLOPs it must do, from the expert counts."""
     H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
     touched = int((counts > 0).sum())
-    # Bytes per GEMM operand element: bf16, or MXFP8's E4M3 code plus its share
-    # of the E8M0 scale (one per 32). x, logits and out are bf16 / fp32 either way.
-    wb = 1 + 1 / 32 if shape.dtype == "mxfp8" else 2
+    # Bytes per GEMM operand element: bf16, or an MX code (E4M3: 1 byte, E2M1:
+    # half a byte) plus its share of the E8M0 scale (one per 32). W4A8 has E2M1
+    # routed weights and E4M3 activations and shared weights. x, logits and out
+    # are bf16 / fp32 either way.
+    mx = shape.dtype in ("mxfp8", "mxfp4")
+    ab = 1 + 1 / 32 if mx else 2                                  # activations, shared weights
+    wb = 0.5 + 1 / 32 if shape.dtype == "mxfp4" else ab           # routed weights
     w_expert = 3 * H * I * wb
-    w_shared = 3 * H * Is * wb
+    w_shared = 3 * H * Is * ab
     layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2)
     flops = 6 * H * I * T * K + 6 * H * Is * T
     TK = T * K
     # GEMM-1 reads the touched experts' gate/up weights and x_perm, and writes h.
-    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * wb + TK * I * wb)
+    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * ab + TK * I * ab)
     return dict(touched=touched, layer_bytes=layer_bytes, flops=flops, gemm1_bytes=gemm1_bytes,
                 gemm1_flops=4 * H * I * TK)
 
@@ -291,7 +295,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     g1_ms = stage_ms["gemm_gate_up"]
-    bound = "hbm" if args.workload in ("decode", "tiny", "mxfp8") else "tensor"
+    bound = "hbm" if args.workload in ("decode", "tiny", "mxfp8", "mxfp4") else "tensor"
     if bound == "hbm":
         achieved = work["gemm1_bytes"] / (g1_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
@@ -307,7 +311,7 @@ def run_ours(args):
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     # route 1, permute 3 + row gather 1, GEMMs 2, shared GEMMs 2, combine 1;
     # MXFP8 adds the quantiser of x and the gather of its scale atoms.
-    launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1 + (2 if shape.dtype == "mxfp8" else 0)
+    launches_per_step = 1 + 4 + 2 + (2 if shape.I_shared else 0) + 1 + (2 if shape.dtype != "bf16" else 0)
 
     result = {
         "metric": METRIC,
@@ -320,8 +324,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8 (E4M3 activations and weights, E8M0 scale per 32 along K, block-scaled tensor "
-                 "cores, fp32 accumulate)" if shape.dtype == "mxfp8" else "bf16",
+        "dtype": {"mxfp8": "mxfp8 (E4M3 activations and weights, E8M0 scale per 32 along K, block-scaled "
+                           "tensor cores, fp32 accumulate)",
+                  "mxfp4": "w4a8 (E2M1 routed-expert weights, E4M3 activations and shared weights, E8M0 "
+                           "scale per 32 along K, block-scaled tensor cores, fp32 accumulate)"}.get(shape.dtype,
+                                                                                                    "bf16"),
         "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
         "config": {
             "workload": (f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer")

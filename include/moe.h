@@ -66,7 +66,9 @@ typedef enum {
 
 typedef enum {
   MOE_BF16 = 0,       /* bf16 operands, fp32 accumulation */
-  MOE_MXFP8_E4M3 = 1  /* E4M3 elements + one E8M0 scale per 32 along K */
+  MOE_MXFP8_E4M3 = 1, /* E4M3 elements + one E8M0 scale per 32 along K */
+  MOE_MXFP4_W4A8 = 2  /* W4A8 ([Hy3] section 8.2): routed-expert weights E2M1 +
+                         E8M0/32 (MXFP4), activations MXFP8, shared expert W8A8 */
 } moe_dtype_t;
 
 /* Layer shape. T tokens, H hidden, E routed experts, K experts per token,
@@ -92,7 +94,11 @@ typedef struct {
  *   s_gate  = atoms of gate and up together (moe_pack_mx_scales(gate, up)),
  *   s_down  = atoms of down (moe_pack_mx_scales(down, NULL)),
  *   s_up    unused (NULL); ss_gate, ss_up, ss_down the same for the shared
- *   expert. Every scale pointer 16-byte aligned. */
+ *   expert. Every scale pointer 16-byte aligned.
+ * MXFP4_W4A8 mode: as MXFP8, except that the routed w_gate, w_up [E, I, H/2]
+ *   and w_down [E, H, I/2] hold packed E2M1 codes (two per byte, element 2j
+ *   in the low nibble; moe_quantize_mxfp4), 32-byte aligned. Their scales and
+ *   the shared expert (E4M3 + atoms) are as in MXFP8 mode. */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
   const uint8_t *s_gate, *s_up, *s_down;
@@ -191,6 +197,8 @@ MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int num_groups, i
  *   GEMM-2, as the W8A8 path quantises every Linear input ([Hy3] section
  *   8.2). Operands and scales go to the block-scaled tensor cores as stored.
  *   H % 128 == 0, I % 128 == 0.
+ * MXFP4_W4A8: w_* hold packed E2M1 codes ([num_groups, I, H/2] and
+ *   [num_groups, H, I/2], 32-byte aligned); scales and a as in MXFP8.
  * offsets (device): [num_groups + 1] int32, non-decreasing, offsets[0] = 0,
  *   offsets[num_groups] <= rows; NULL means one group of all rows (a dense
  *   SwiGLU MLP, used for the shared expert).
@@ -223,6 +231,17 @@ MOE_API moe_status_t moe_combine(moe_handle_t h, const moe_config_t* cfg, const 
  * in (device): [rows, cols] bf16; q (device): [rows, cols] uint8 out;
  * scale (device): [rows, cols/32] uint8 out. cols % 32 == 0. */
 MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int64_t rows,
+                                        int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream);
+
+/* MXFP4 quantisation of a bf16 matrix along its rows (the W4A8 routed-expert
+ * weights of [Hy3] section 8.2; rule of the OCP MX v1.0 spec with E2M1
+ * elements): per block of 32, scale X = 2^(floor(log2 amax) - 2) stored as
+ * E8M0, elements rounded to nearest-even on the E2M1 grid (0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6) saturating at +-6; an all-zero block gets scale code 0.
+ * in (device): [rows, cols] bf16; q (device): [rows, cols/2] uint8 out, two
+ * codes per byte (element 2j in the low nibble); scale (device): [rows,
+ * cols/32] uint8 out. cols % 32 == 0. */
+MOE_API moe_status_t moe_quantize_mxfp4(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream);
 
 /* Scale atoms for the block-scaled MXFP8 GEMM from row-major E8M0 scales

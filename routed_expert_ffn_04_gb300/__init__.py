@@ -5,7 +5,7 @@ ABI of include/moe.h. PyTorch provides device memory and streams. The binding
 refuses to run when the compiled library is missing; there is no CPU path.
 
 Names follow the C ABI: route, permute, grouped_swiglu_gemm, combine,
-quantize_mxfp8, layer_forward, layer_forward_host.
+quantize_mxfp8, quantize_mxfp4, pack_mx_scales, layer_forward, layer_forward_host.
 """
 from __future__ import annotations
 
@@ -22,7 +22,8 @@ LIB_PATH = _build.LIB
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = range(6)
-MOE_BF16, MOE_MXFP8_E4M3 = 0, 1
+MOE_BF16, MOE_MXFP8_E4M3, MOE_MXFP4_W4A8 = 0, 1, 2
+DTYPES = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8_E4M3, "mxfp4": MOE_MXFP4_W4A8}
 MOE_OPT_GEMM_MODE, MOE_OPT_STAGE_TIMING, MOE_OPT_WAIT_LIMIT_US = 0, 1, 2
 STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine", "shared", "total"]
 DEV_TIMEOUT_SELFTEST = 4
@@ -79,6 +80,7 @@ def load(build_if_missing: bool = False):
         "moe_grouped_swiglu_gemm": [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, S, P],
         "moe_combine": [P, P, P, P, P, P, P, P],
         "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
+        "moe_quantize_mxfp4": [P, P, ctypes.c_int64, I, P, P, P],
         "moe_pack_mx_scales": [P, P, P, ctypes.c_int64, I, P, P],
         "moe_layer_forward": [P, P, P, P, P, P, P, S, P, P],
         "moe_layer_forward_host": [P, P, P, P, P, P, P, S, P, P],
@@ -239,11 +241,27 @@ def quantize_mx(h: Handle, t, stream=None):
     return q, sc
 
 
-def quantize_weights_mx(h: Handle, w: dict, stream=None) -> dict:
-    """MX form of a bf16 weight dict: w_* -> E4M3 codes, s_* / ss_* -> row-major scales."""
+def quantize_mxfp4(h: Handle, x, q, scale, stream=None):
+    rows = x.numel() // x.shape[-1]
+    _check(load().moe_quantize_mxfp4(h.ptr, _p(x), int(rows), int(x.shape[-1]), _p(q), _p(scale), _stream(stream)),
+           "moe_quantize_mxfp4")
+
+
+def quantize_mx4(h: Handle, t, stream=None):
+    """MXFP4 packed E2M1 codes (uint8, last dim / 2) and E8M0 scales (uint8, last dim / 32) of a bf16 tensor."""
+    q = torch.empty(t.shape[:-1] + (t.shape[-1] // 2,), dtype=torch.uint8, device=t.device)
+    sc = torch.empty(t.shape[:-1] + (t.shape[-1] // 32,), dtype=torch.uint8, device=t.device)
+    quantize_mxfp4(h, t, q, sc, stream=stream)
+    return q, sc
+
+
+def quantize_weights_mx(h: Handle, w: dict, stream=None, w4: bool = False) -> dict:
+    """MX form of a bf16 weight dict: w_* -> E4M3 codes (w4: routed w_* -> packed
+    E2M1 codes, the W4A8 recipe; the shared ws_* stay E4M3), s_* / ss_* ->
+    row-major scales."""
     out = {}
     for k, v in w.items():
-        q, sc = quantize_mx(h, v, stream=stream)
+        q, sc = (quantize_mx4 if (w4 and k.startswith("w_")) else quantize_mx)(h, v, stream=stream)
         out[k] = q
         out[("ss_" + k[3:]) if k.startswith("ws_") else ("s_" + k[2:])] = sc
     return out
@@ -317,12 +335,12 @@ class MoELayer:
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.shape = shape
         self.cfg = make_config(shape.T, shape.H, shape.E, shape.K, shape.I, shape.I_shared, shape.scaling,
-                               shape.route_norm, MOE_MXFP8_E4M3 if shape.dtype == "mxfp8" else MOE_BF16)
+                               shape.route_norm, DTYPES[shape.dtype])
         self.handle = Handle(self.device.index)
         self.ws = torch.empty(workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
-        if shape.dtype == "mxfp8":
+        if shape.dtype in ("mxfp8", "mxfp4"):
             if weights["w_gate"].dtype != torch.uint8:
-                weights = quantize_weights_mx(self.handle, weights)
+                weights = quantize_weights_mx(self.handle, weights, w4=shape.dtype == "mxfp4")
             if weights.get("s_up") is not None:  # row-major scales -> scale atoms
                 weights = pack_weights_mx(self.handle, weights)
             torch.cuda.synchronize(self.device)

@@ -46,6 +46,14 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool is_mx(int dtype) { return dtype == MOE_MXFP8_E4M3 || dtype == MOE_MXFP4_W4A8; }
+
+// Packed E2M1 weights are read through tensor maps that need 32-byte bases.
+bool weights_aligned32(const void* a, const void* b, const void* c) {
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+           reinterpret_cast<uintptr_t>(c)) & 31) == 0;
+}
+
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 moe_status_t check_cfg(const moe_config_t* c) {
@@ -57,9 +65,9 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if ((long long)c->T * c->K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
   const long long wide = c->H > c->I ? c->H : c->I;
   if ((long long)c->T * c->K * wide >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
-  if (c->dtype != MOE_BF16 && c->dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  // MXFP8: whole scale atoms (128 x 128) along H, I and I_shared.
-  if (c->dtype == MOE_MXFP8_E4M3 && (c->H % 128 || c->I % 128 || c->I_shared % 128))
+  if (c->dtype != MOE_BF16 && !is_mx(c->dtype)) return MOE_ERR_INVALID_ARG;
+  // MX: whole scale atoms (128 x 128) along H, I and I_shared.
+  if (is_mx(c->dtype) && (c->H % 128 || c->I % 128 || c->I_shared % 128))
     return MOE_ERR_INVALID_ARG;
   if (!(c->scaling == c->scaling)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -90,7 +98,7 @@ Layout layout_of(const moe_config_t* c) {
   L.perm_src = take(TK * 4);
   L.flat_to_perm = take(TK * 4);
   L.perm_scratch = take(permute_scratch_bytes((int)TK, (int)E));
-  const bool mx = c->dtype == MOE_MXFP8_E4M3;
+  const bool mx = is_mx(c->dtype);
   const size_t eb = mx ? 1 : 2;  // bytes per activation element (E4M3 codes or bf16)
   L.x_perm = take(TK * H * eb);
   L.h = take(TK * I * eb);
@@ -125,8 +133,7 @@ moe_status_t check_handle(moe_handle_t h) {
 
 GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int rows, int H, int I,
                           const void* a, const void* wg, const void* wu, const void* wd, void* hbuf,
-                          float* y, const uint8_t* sg = nullptr, const uint8_t* su = nullptr,
-                          const uint8_t* sd = nullptr) {
+                          float* y, const uint8_t* sg = nullptr, const uint8_t* sd = nullptr) {
   GroupedGemmArgs g;
   g.a_scale = nullptr;
   g.h_scale = nullptr;
@@ -135,10 +142,9 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
   g.topk = 0;
   g.scaling = 1.0f;
   g.route_norm = 0;
-  g.mx = sg != nullptr;
   g.s_gate = sg;
-  g.s_up = su;
   g.s_down = sd;
+  g.w4 = 0;
   g.G = G;
   g.offsets = offsets;
   g.rows = rows;
@@ -305,7 +311,7 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
                                  moe_stream_t stream) {
   moe_status_t st = check_cfg(cfg);
   if (st != MOE_OK) return st;
-  const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
+  const bool mx = is_mx(cfg->dtype);
   const bool any = cfg->T > 0;
   if (!counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
   if (any && (!x || !topk_idx || !perm_src || !flat_to_perm || !x_perm)) return MOE_ERR_INVALID_ARG;
@@ -347,8 +353,8 @@ GemmWs gemm_ws(int rows, int groups, int H, int I, bool mx) {
 MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int num_groups, int H, int I,
                                                      moe_dtype_t dtype, size_t* bytes) {
   if (!bytes || rows < 0 || num_groups <= 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
-  if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  *bytes = gemm_ws(rows, num_groups, H, I, dtype == MOE_MXFP8_E4M3).total;
+  if (dtype != MOE_BF16 && !is_mx(dtype)) return MOE_ERR_INVALID_ARG;
+  *bytes = gemm_ws(rows, num_groups, H, I, is_mx(dtype)).total;
   return MOE_OK;
 }
 
@@ -363,10 +369,12 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
     return MOE_ERR_INVALID_ARG;
   if (offsets == nullptr && num_groups != 1) return MOE_ERR_INVALID_ARG;
   if ((long long)rows * (H > I ? H : I) >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
-  if (dtype != MOE_BF16 && dtype != MOE_MXFP8_E4M3) return MOE_ERR_INVALID_ARG;
-  const bool mx = dtype == MOE_MXFP8_E4M3;
+  if (dtype != MOE_BF16 && !is_mx(dtype)) return MOE_ERR_INVALID_ARG;
+  const bool mx = is_mx(dtype);
+  const bool w4 = dtype == MOE_MXFP4_W4A8;
   if (!a || !w_gate || !w_up || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (mx && (!a_scale || !s_gate || !s_down || H % 128 || I % 128)) return MOE_ERR_INVALID_ARG;
+  if (w4 && !weights_aligned32(w_gate, w_up, w_down)) return MOE_ERR_INVALID_ARG;
   (void)s_up;  // MXFP8: s_gate holds the gate and up scale atoms together
   const void* ptrs[] = {a, offsets, w_gate, w_up, w_down, y, ws, s_gate, s_down};
   for (const void* p : ptrs)
@@ -377,7 +385,8 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   GroupedGemmArgs g = gemm_args(h, num_groups, offsets, rows, H, I, a, w_gate, w_up, w_down, ws, y,
-                                mx ? s_gate : nullptr, nullptr, mx ? s_down : nullptr);
+                                mx ? s_gate : nullptr, mx ? s_down : nullptr);
+  g.w4 = w4;
   cudaError_t e = cudaSuccess;
   if (mx) {  // block-scaled tensor cores; h stays E4M3 + E8M0 between the GEMMs
     uint8_t* a_atoms = at<uint8_t>(ws, W.a_atoms);
@@ -421,6 +430,16 @@ MOE_API moe_status_t moe_pack_mx_scales(moe_handle_t h, const uint8_t* scale0,
       launch_pack_weight_scales(scale0, scale1, rows, cols, atoms, static_cast<cudaStream_t>(stream)));
 }
 
+MOE_API moe_status_t moe_quantize_mxfp4(moe_handle_t h, const void* in_bf16, int64_t rows,
+                                        int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!in_bf16 || !q || !scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(in_bf16) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_handle(h);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_mx4_quantize(in_bf16, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
+}
+
 MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
@@ -445,8 +464,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (!aligned16(w_router)) return MOE_ERR_INVALID_ARG;
   if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
-  const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
+  const bool mx = is_mx(cfg->dtype);
+  const bool w4 = cfg->dtype == MOE_MXFP4_W4A8;  // routed experts E2M1; shared stays E4M3
   if (mx && (!w->s_gate || !w->s_down)) return MOE_ERR_INVALID_ARG;
+  if (w4 && !weights_aligned32(w->w_gate, w->w_up, w->w_down)) return MOE_ERR_INVALID_ARG;
   if (mx && has_shared && (!w->ss_gate || !w->ss_down)) return MOE_ERR_INVALID_ARG;
   if (mx && (!aligned16(w->s_gate) || !aligned16(w->s_down) || !aligned16(w->ss_gate) ||
              !aligned16(w->ss_down)))
@@ -507,7 +528,7 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     }
     mark(6, s_sh);
     GroupedGemmArgs g = gemm_args(h, 1, nullptr, T, H, Is, x, w->ws_gate, w->ws_up, w->ws_down,
-                                  h_shared, s_out, mx ? w->ss_gate : nullptr, nullptr,
+                                  h_shared, s_out, mx ? w->ss_gate : nullptr,
                                   mx ? w->ss_down : nullptr);
     if (mx) {
       g.a_scale = at<uint8_t>(ws, L.x_mx_atoms);
@@ -538,8 +559,9 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
                                   at<uint8_t>(ws, L.x_perm_s), h->status, sm);
   mark(2, sm);
   GroupedGemmArgs g = gemm_args(h, E, offsets, TK, H, I, x_perm, w->w_gate, w->w_up, w->w_down,
-                                hbuf, y_perm, mx ? w->s_gate : nullptr, nullptr,
+                                hbuf, y_perm, mx ? w->s_gate : nullptr,
                                 mx ? w->s_down : nullptr);
+  g.w4 = w4;
   if (mx) {
     g.a_scale = at<uint8_t>(ws, L.x_perm_s);
     g.h_scale = at<uint8_t>(ws, L.h_s);

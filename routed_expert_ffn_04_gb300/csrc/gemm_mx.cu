@@ -9,6 +9,12 @@
 //                    32 along I and stored as E4M3 codes + E8M0 scales
 //   GEMM-2 (MODE 1): y = h Wd^T, fp32
 //
+// W4 (the W4A8 recipe of the same section: MXFP4 routed-expert weights, MXFP8
+// activations): the weights are packed E2M1, TMA-loaded through a 16U4 tensor
+// map that puts each 16 codes in the low half of a 16-byte slot, the operand
+// layout kind::mxf8f6f4 reads for E2M1 (B format code 5). Shared-memory tiles,
+// scales and the MMA shape are those of E4M3; HBM weight bytes halve.
+//
 // Scales travel in scale atoms (mx_layout.cuh): 512 bytes per 128 rows x 128
 // K elements, already in the order the block-scaled MMA reads from TMEM.
 // A stage's two atoms (A rows, B rows) ride on the same mbarrier as its TMA
@@ -60,12 +66,16 @@ static_assert(kSfCol0 + 8 * kStages <= kTmemCols, "TMEM budget");
 static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
 static_assert(kTableBytes % 16 == 0 && kEpiBytes % 16 == 0, "scale atoms need 16-byte alignment");
 
-template <int MODE>
+template <int MODE, bool W4>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_act,
                            const __grid_constant__ CUtensorMap map_w0,
                            const __grid_constant__ CUtensorMap map_w1, const KParams p) {
   constexpr int W_COLS = MODE == 0 ? 64 : 128;  // output columns per tile
+  // Transaction bytes of a stage: the A tile, the two B boxes (E2M1 boxes count
+  // their packed global bytes, half the shared-memory footprint), the atoms.
+  constexpr uint32_t kStageTx = kTileBytes + (W4 ? kTileBytes / 2 : kTileBytes) + kSfBytes;
+  constexpr uint32_t kIdescFmt = W4 ? (5u << 10) : 0u;  // B format: E2M1 or E4M3
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
@@ -168,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = full_bar(rg.s);
-          mbar_arrive_expect_tx(fb, kStageBytes + kSfBytes);
+          mbar_arrive_expect_tx(fb, kStageTx);
           const uint32_t st = stage0 + rg.s * kStageBytes;
           const uint32_t sf = sf_smem0 + rg.s * kSfBytes;
           const int kx = kb * kK;
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             umma_mxf8(d, sw128_kmajor_desc(st + k * 32), sw128_kmajor_desc(st + kTileBytes + k * 32),
-                      idesc_mxf8_e4m3(128, 128, k, k), sf, sf + 4, (kb | k) ? 1u : 0u);
+                      idesc_mxf8_e4m3(128, 128, k, k) | kIdescFmt, sf, sf + 4, (kb | k) ? 1u : 0u);
           }
           issued = true;
           umma_commit(empty_bar(rg.s));
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE>
+template <int MODE, bool W4>
 cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   const int Kdim = MODE == 0 ? a.H : a.I;
   const int N = MODE == 0 ? a.I : a.H;
@@ -340,9 +350,9 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.H % 128 || a.I % 128 || a.G > kMaxGroups) return cudaErrorInvalidValue;
   const int G = a.offsets ? a.G : 1;
   CUtensorMap m_act, m_w0, m_w1;
-  if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) ||
-      !make_tmap_u8(&m_w0, w0, Kdim, (uint64_t)G * N, 64) ||
-      !make_tmap_u8(&m_w1, w1, Kdim, (uint64_t)G * N, 64))
+  auto wmap = W4 ? make_tmap_e2m1 : make_tmap_u8;
+  if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) || !wmap(&m_w0, w0, Kdim, (uint64_t)G * N, 64) ||
+      !wmap(&m_w1, w1, Kdim, (uint64_t)G * N, 64))
     return cudaErrorInvalidValue;
   KParams p = {};
   p.offsets = a.offsets;
@@ -360,27 +370,29 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long n_wt = (N + W_COLS - 1) / W_COLS;
   const long long max_tiles = n_wt * ((a.rows + 127) / 128 + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
-  grouped_gemm_mx_kernel<MODE><<<grid, kThreads, kSmem, s>>>(m_act, m_w0, m_w1, p);
+  grouped_gemm_mx_kernel<MODE, W4><<<grid, kThreads, kSmem, s>>>(m_act, m_w0, m_w1, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t gemm_mx_prepare_device() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<0>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem);
-  return e;
+  const cudaError_t errs[] = {
+      cudaFuncSetAttribute(grouped_gemm_mx_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)};
+  for (cudaError_t e : errs)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
-  return run_gemm_mx<0>(a, s);
+  return a.w4 ? run_gemm_mx<0, true>(a, s) : run_gemm_mx<0, false>(a, s);
 }
 
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s) {
-  return run_gemm_mx<1>(a, s);
+  return a.w4 ? run_gemm_mx<1, true>(a, s) : run_gemm_mx<1, false>(a, s);
 }
 
 }  // namespace moe

@@ -20,13 +20,9 @@ struct KParams {
   void* out;     // bf16 h (MODE 0) or fp32 y (MODE 1)
   int* status;
   uint64_t limit_ns;
-  // MXFP8 weights (WQ): E8M0 scales [G*N, Kdim/32] for the two weight maps.
+  // MXFP8 (gemm_mx.cu): scale atoms of the weights, of the activations (one
+  // atom row-block per token tile), and for GEMM-1 of the E4M3 h it writes.
   const uint8_t* s_w0;
-  const uint8_t* s_w1;
-  int sstride;   // Kdim / 32
-  int w_rows;    // G * N
-  // Native MXFP8 (gemm_mx.cu): activation E8M0 scales [rows, Kdim/32], and
-  // for GEMM-1 the scales of the E4M3 h it writes ([rows, N/32]).
   const uint8_t* s_act;
   uint8_t* out_scale;
   // Gating (MODE 2): routing outputs [rows, topk]; `out` (nullable) takes the logits.

@@ -54,15 +54,14 @@ struct GroupedGemmArgs {
   float scaling;
   int route_norm;
   int mode;                // GemmMode
-  int mx;                  // 1: weights are E4M3 + E8M0/32 (h MX-rounded too)
-  // Native MXFP8 (gemm_mx.cu): a / h hold E4M3 codes, their scales are atoms
-  // by token tile of each group; s_gate the gate/up atoms, s_down the down atoms.
-  // The WQ converter path of gemm.cu reads s_gate, s_up, s_down row-major.
+  // MXFP8 (gemm_mx.cu): a / h hold E4M3 codes and their scales are atoms by
+  // token tile of each group; s_gate the gate/up atoms, s_down the down atoms.
+  // w4: the weights are packed E2M1 (two per byte, MXFP4) instead of E4M3.
   const uint8_t* a_scale;
   uint8_t* h_scale;
   const uint8_t* s_gate;
-  const uint8_t* s_up;
   const uint8_t* s_down;
+  int w4;
   int num_sms;
   int* status;
   uint64_t wait_limit_ns;
@@ -73,6 +72,12 @@ bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailab
 cudaError_t gemm_prepare_device();
 // 2-D uint8 tensor map [outer, inner], box {128 bytes, box_rows}, 128-byte swizzle.
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
+// 2-D packed E2M1 tensor map [outer, inner elements] (inner / 2 bytes per row;
+// inner % 128 == 0, ptr 32-byte aligned), box {128 elements, box_rows}: each
+// 16 codes (8 bytes) land in the low half of a 16-byte shared-memory slot,
+// 128-byte swizzle, the operand layout of kind::mxf8f6f4 for E2M1. The
+// transaction count of a box is its global bytes (64 per row).
+bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
 // Native MXFP8 grouped GEMM (gemm_mx.cu): block-scaled tcgen05 MMA, E4M3
 // activations (a + a_scale; GEMM-2 reads h + h_scale) and weights.
 cudaError_t gemm_mx_prepare_device();
@@ -97,6 +102,11 @@ cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32
 // dequantised values as bf16.
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
                                uint8_t* scale, uint8_t* atoms, void* deq, cudaStream_t s);
+
+// MXFP4: q [rows, cols/2] packed E2M1 codes (element 2j in the low nibble),
+// scale [rows, cols/32] row-major.
+cudaError_t launch_mx4_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
+                                uint8_t* scale, cudaStream_t s);
 
 // ---- scale atoms (mxpack.cu; layout in mx_layout.cuh)
 // Row-major E8M0 scales [rows, cols/32] -> atoms. s1 == nullptr: the atoms

@@ -1,10 +1,9 @@
 // MXFP8 element helpers (E4M3 elements, E8M0 block scales; OCP MX v1.0):
-// exact expansion of scaled E4M3 codes into bf16, and the quantise ->
-// dequantise round trip of the OCP MX conversion rule.
+// the block shared exponent and element encoding of the OCP MX conversion
+// rule, and the exact expansion of scaled E4M3 codes into bf16.
 #pragma once
 
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include <cstdint>
@@ -50,43 +49,6 @@ __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, int sc, uint32_t& lo,
   }
 }
 
-// Sixteen E4M3 codes (one 16-byte chunk) times 2^(sc - 127) -> sixteen bf16,
-// stored as two 16-byte vectors at d0 (elements 0-7) and d1 (elements 8-15).
-// The exact-but-slow per-code path is kept out of line; it only runs for
-// chunks holding zero/subnormal codes or extreme scales.
-static __device__ __noinline__ void e4m3x16_to_bf16_slow(uint4 c, int sc, uint4* d0, uint4* d1) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-  uint32_t o[8];
-  for (int k = 0; k < 4; ++k)
-    for (int b = 0; b < 4; b += 2)
-      o[2 * k + b / 2] = e4m3_scaled_bf16_slow((w[k] >> (8 * b)) & 0xFFu, sc) |
-                         (e4m3_scaled_bf16_slow((w[k] >> (8 * b + 8)) & 0xFFu, sc) << 16);
-  *d0 = make_uint4(o[0], o[1], o[2], o[3]);
-  *d1 = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void e4m3x16_to_bf16_store(uint4 c, int sc, uint4* d0, uint4* d1) {
-  const uint32_t e0 = c.x & 0x78787878u, e1 = c.y & 0x78787878u, e2 = c.z & 0x78787878u,
-                 e3 = c.w & 0x78787878u;
-  const uint32_t z = ((e0 - 0x08080808u) & ~e0) | ((e1 - 0x08080808u) & ~e1) |
-                     ((e2 - 0x08080808u) & ~e2) | ((e3 - 0x08080808u) & ~e3);
-  if ((z & 0x80808080u) == 0u && sc >= 8 && sc <= 245) {
-    const uint32_t add = (uint32_t)(sc - 7) * 0x00800080u;
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t x0 = __byte_perm(w[k], 0u, 0x4140), x1 = __byte_perm(w[k], 0u, 0x4342);
-      o[2 * k] = (((x0 & 0x007F007Fu) << 4) + add) | ((x0 & 0x00800080u) << 8);
-      o[2 * k + 1] = (((x1 & 0x007F007Fu) << 4) + add) | ((x1 & 0x00800080u) << 8);
-    }
-    *d0 = make_uint4(o[0], o[1], o[2], o[3]);
-    *d1 = make_uint4(o[4], o[5], o[6], o[7]);
-  } else {
-    e4m3x16_to_bf16_slow(c, sc, d0, d1);
-  }
-}
-
 // Block shared exponent of the OCP MX rule: floor(log2 amax) - 8, clamped to
 // [-127, 127]. amax must be > 0.
 __device__ __forceinline__ int mx_shared_exp(float amax) {
@@ -98,13 +60,23 @@ __device__ __forceinline__ uint32_t mx_encode(float v, int sexp) {
   return (uint32_t)__nv_cvt_float_to_fp8(v * pow2f(-sexp), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Quantise v (in a block whose amax is given) to E4M3 and return the
-// dequantised value (exact in bf16). amax == 0 gives +0.
-__device__ __forceinline__ float mx_roundtrip(float v, float amax) {
-  if (amax == 0.0f) return 0.0f;
-  const int sexp = mx_shared_exp(amax);
-  const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)mx_encode(v, sexp), __NV_E4M3);
-  return __half2float(__half(hr)) * pow2f(sexp);
+// MXFP4 (E2M1 elements, [OCP-MX] rule with emax_elem = 2): shared exponent
+// floor(log2 amax) - 2, clamped to [-127, 127]. amax must be > 0.
+__device__ __forceinline__ int mx4_shared_exp(float amax) {
+  int sexp = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;
+  return sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
+}
+
+// E2M1 code (4 bits) of v / X, X = 2^sexp: round to nearest on the grid
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code (mantissa bit 0),
+// saturating at 6. Each midpoint comparison is against t * X, exact in fp32
+// for every X >= 2^-127, so no division is rounded. The sign bit follows v.
+__device__ __forceinline__ uint32_t e2m1_encode(float v, float X) {
+  const float a = fabsf(v);
+  const uint32_t code = (uint32_t)(a > 0.25f * X) + (uint32_t)(a >= 0.75f * X) +
+                        (uint32_t)(a > 1.25f * X) + (uint32_t)(a >= 1.75f * X) +
+                        (uint32_t)(a > 2.5f * X) + (uint32_t)(a >= 3.5f * X) + (uint32_t)(a > 5.0f * X);
+  return code | ((__float_as_uint(v) >> 28) & 8u);
 }
 
 }  // namespace moe

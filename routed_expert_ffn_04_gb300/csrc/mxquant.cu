@@ -6,6 +6,9 @@
 //   shared_exp = floor(log2(amax)) - 8   (8 = largest E4M3 exponent)
 //   scale code = clamp(shared_exp, -127, 127) + 127;  amax == 0 -> code 0
 //   element    = RNE(v / 2^shared_exp) to E4M3, saturating at +-448
+// MXFP4 (the W4A8 routed-expert weights of section 8.2) follows the same rule
+// with E2M1 elements (emax_elem = 2, saturating at +-6), two codes per byte.
+//
 // One thread per block of 32: 64 bytes in (four 16-byte loads), 32 code
 // bytes out (two 16-byte stores) and one scale byte, row-major and/or in the
 // scale atoms of the block-scaled GEMM (mx_layout.cuh); optionally the
@@ -76,6 +79,37 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
   }
 }
 
+// MXFP4: one thread per block of 32 bf16 -> 16 bytes of packed E2M1 codes
+// (element 2j in the low nibble) and one E8M0 scale byte.
+__global__ void __launch_bounds__(256) mx4_quant_kernel(const uint4* __restrict__ in,
+                                                        long long nblocks, uint4* __restrict__ q,
+                                                        uint8_t* __restrict__ scale) {
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nblocks) return;
+  uint4 raw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) raw[j] = __ldg(in + b * 4 + j);
+  const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(raw);
+  float f[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    f[j] = __bfloat162float(v[j]);
+    amax = fmaxf(amax, fabsf(f[j]));
+  }
+  uint32_t words[4] = {0u, 0u, 0u, 0u};
+  int code = 0;
+  if (amax != 0.0f) {
+    const int sexp = mx4_shared_exp(amax);
+    code = sexp + 127;
+    const float X = pow2f(sexp);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) words[j >> 3] |= e2m1_encode(f[j], X) << (4 * (j & 7));
+  }
+  scale[b] = (uint8_t)code;
+  q[b] = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
 __global__ void __launch_bounds__(256) mx_dequant_kernel(const uint4* __restrict__ q,
                                                          const uint8_t* __restrict__ scale,
                                                          long long nblocks,
@@ -103,6 +137,16 @@ cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint
   mx_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
                                                  reinterpret_cast<uint4*>(q), scale, atoms,
                                                  cols / 32, static_cast<uint4*>(deq));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx4_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
+                                uint8_t* scale, cudaStream_t s) {
+  const long long nblocks = (long long)rows * (cols / 32);
+  if (nblocks == 0) return cudaSuccess;
+  const long long grid = (nblocks + 255) / 256;
+  mx4_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
+                                                  reinterpret_cast<uint4*>(q), scale);
   return cudaGetLastError();
 }
 

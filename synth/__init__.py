@@ -39,7 +39,7 @@ class MoEShape:
     I_shared: int
     scaling: float = SCALING_HY3
     route_norm: bool = True
-    dtype: str = "bf16"  # "bf16" or "mxfp8"
+    dtype: str = "bf16"  # "bf16", "mxfp8" (W8A8) or "mxfp4" (W4A8: MXFP4 routed weights)
     skew: bool = False
 
     def as_dict(self):
@@ -62,6 +62,9 @@ WORKLOADS = {
     "skewed": MoEShape("skewed", T=4096, H=4096, E=256, K=8, I=1536, I_shared=1536, skew=True),
     # Hy3 shape in MXFP8 (E4M3 + E8M0 per 32 along K).
     "mxfp8": MoEShape("mxfp8", T=2048, H=4096, E=192, K=8, I=1536, I_shared=1536, dtype="mxfp8"),
+    # The same in W4A8: routed-expert weights MXFP4 (E2M1 + E8M0/32), MXFP8
+    # activations, shared expert W8A8 ([Hy3] section 8.2).
+    "mxfp4": MoEShape("mxfp4", T=2048, H=4096, E=192, K=8, I=1536, I_shared=1536, dtype="mxfp4"),
 }
 
 _STREAMS = dict(x=1, logits=2, bias=3, w_gate=4, w_up=5, w_down=6, ws_gate=7, ws_up=8, ws_down=9)

@@ -54,6 +54,19 @@ def test_mx_config_needs_whole_scale_atoms(lib):
     assert lib.moe_workspace_size(ctypes.byref(_cfg(dtype=moe.MOE_MXFP8_E4M3)), ctypes.byref(n)) == moe.MOE_OK
 
 
+def test_w4a8_weights_need_32_byte_alignment(lib):
+    P = ctypes.c_void_p
+    args = lambda wg: (None, 1, 128, 256, 128, moe.MOE_MXFP4_W4A8, P(256), P(256), None, P(wg), P(512), P(512),
+                       P(256), None, P(256), P(256), P(256), 1 << 30, None)
+    # Packed E2M1 weights at a 16- but not 32-byte-aligned address: rejected before any launch.
+    assert lib.moe_grouped_swiglu_gemm(*args(528)) == moe.MOE_ERR_INVALID_ARG
+    # Aligned: passes the argument checks and stops at the null handle (also INVALID_ARG), so
+    # check the workspace path instead: a too-small workspace is reported as such.
+    small = list(args(512))
+    small[17] = 16
+    assert lib.moe_grouped_swiglu_gemm(*small) == moe.MOE_ERR_WORKSPACE
+
+
 def test_pack_mx_scales_argument_checks(lib):
     P = ctypes.c_void_p
     # cols not a multiple of 128, rows not a multiple of 128 (single) or 64 (pair), misaligned pointer.
