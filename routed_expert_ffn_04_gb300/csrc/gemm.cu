@@ -65,9 +65,12 @@ struct Geo {
                                    : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
   static constexpr int TABLE_BYTES = (kMaxGroups + 8) * 4;
   static constexpr int BAR_BYTES = 512;
-  // Tokens-as-M epilogue: per-warp 32 x 32 fp32 staging (row stride 33) so
-  // output rows leave as contiguous 128-byte stores.
-  static constexpr int EPI_BYTES = SWAP ? 0 : 4 * 32 * 33 * 4;
+  // Tokens-as-M epilogue: a per-warp 32 x 32 fp32 staging block. GEMM-2 stores
+  // it by TMA (4 KB, 128-byte swizzled, 1024-aligned: 5 KB per warp, which also
+  // fits the row-stride-33 layout of its row-by-row path); the others use the
+  // row-stride-33 layout only.
+  static constexpr int EPI_WARP = MODE == 1 ? 5120 : 32 * 33 * 4;
+  static constexpr int EPI_BYTES = SWAP ? 0 : 4 * EPI_WARP;
   static constexpr int EXTRA = 1024 + TABLE_BYTES + BAR_BYTES + EPI_BYTES;
   static constexpr int BUDGET = kMaxSmem - EXTRA;
   // One ring whose stages hold both operands of a K slice.
@@ -81,6 +84,7 @@ struct Geo {
   static constexpr int NBARS = 2 * S_AB + 5;
   static_assert(S_AB >= 2, "shared memory too small for two stages");
   static_assert(ACT_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "1024-byte alignment of swizzled stages");
+  static_assert(EPI_BYTES % 16 == 0, "staging keeps the table aligned");
   static_assert(SMEM <= kMaxSmem, "shared memory budget");
   static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(!SWAP || (BN % 32 == 0 && BN >= 32 && BN <= 128), "token tile");
@@ -91,7 +95,7 @@ struct Geo {
 // 32 lanes.
 template <bool SWAP, int MODE, int BN>
 __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& ti, uint32_t tb,
-                                              int q, int lane, float* stg) {
+                                              int q, int lane, float* stg, const CUtensorMap* map_y) {
   if (SWAP) {
     // TMEM lane = weight row (output column), TMEM column = token.
     const int r_first = ti.tt * BN;
@@ -196,10 +200,15 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
         }
       }
     } else {
-      // fp32 y: each 32 x 32 block goes through the warp's staging tile so
-      // that every store instruction writes 128 contiguous bytes of one row.
+      // fp32 y, 32 x 32 blocks per warp. When all 32 rows belong to the group
+      // the block leaves by one TMA bulk store from a 128-byte-swizzled 4 KB
+      // buffer (16-byte chunk j of row r at chunk j ^ (r % 8)). A block that
+      // crosses the group's end goes row by row through the row-stride-33
+      // layout, since a TMA box would also write rows of the next group.
       const int r_first = ti.tt * 128 + q * 32;  // this warp's first row in the group
+      const bool whole = r_first + 32 <= ti.nrows;
       float* y = static_cast<float*>(p.out);
+      const uint32_t stg_u32 = smem_u32(stg);
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         uint32_t v[32];
@@ -207,15 +216,31 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
         tmem_ld_wait();
         const int col = ti.wt * 256 + c;
         if (col < p.N) {  // warp-uniform
+          if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
+          __syncwarp();
+          if (whole) {
+            uint8_t* row = reinterpret_cast<uint8_t*>(stg) + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
-          __syncwarp();
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(map_y, stg_u32, col, ti.row0 + r_first);
+              bulk_commit_group();
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
+            __syncwarp();
 #pragma unroll 4
-          for (int rr = 0; rr < 32; ++rr) {
-            const int row = r_first + rr;
-            if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+            for (int rr = 0; rr < 32; ++rr) {
+              const int row = r_first + rr;
+              if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
     }
@@ -226,16 +251,18 @@ template <bool SWAP, int MODE, int BN>
 __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
                         const __grid_constant__ CUtensorMap map_w0,
-                        const __grid_constant__ CUtensorMap map_w1, const KParams p) {
+                        const __grid_constant__ CUtensorMap map_w1,
+                        const __grid_constant__ CUtensorMap map_y, const KParams p) {
   using Gm = Geo<SWAP, MODE, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
   uint8_t* base = smem_raw + pad;
   const uint32_t base_u32 = raw_addr + pad;
-  int32_t* tile_start = reinterpret_cast<int32_t*>(base + Gm::RING_BYTES);
-  float* epi_stage = reinterpret_cast<float*>(base + Gm::RING_BYTES + Gm::TABLE_BYTES + Gm::BAR_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::RING_BYTES + Gm::TABLE_BYTES);
+  // Shared memory: ring | epilogue staging (1024-aligned) | tile table | barriers.
+  float* epi_stage = reinterpret_cast<float*>(base + Gm::RING_BYTES);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(base + Gm::RING_BYTES + Gm::EPI_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::RING_BYTES + Gm::EPI_BYTES + Gm::TABLE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Gm::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -412,11 +439,12 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
       tc_fence_after();
       const TileInfo ti = decode_tile<Gm::ACT_ROWS>(p, tile_start, tile);
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Gm::ACC_COLS);
-      epilogue_tile<SWAP, MODE, BN>(p, ti, tb, q, lane, epi_stage + q * 32 * 33);
+      epilogue_tile<SWAP, MODE, BN>(p, ti, tb, q, lane, epi_stage + q * (Gm::EPI_WARP / 4), &map_y);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's bulk stores are complete
   }
 
   tc_fence_before();
@@ -467,6 +495,20 @@ bool make_map(CUtensorMap* m, const void* ptr, bool fp8, uint64_t inner, uint64_
   return r == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor [outer, inner], box {32, 32} (128-byte rows), 128-byte
+// swizzle: the staging block of the GEMM-2 epilogue's bulk stores.
+bool make_map_f32(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer) {
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
@@ -498,7 +540,7 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const void* w1 = MODE == 0 ? a.w_up : a.w_down;
   if (a.rows == 0 || a.G == 0) return cudaSuccess;
   const int G = a.offsets ? a.G : 1;
-  CUtensorMap m_act, m_w0, m_w1;
+  CUtensorMap m_act, m_w0, m_w1, m_y;
   if (!make_map(&m_act, act, false, Kdim, a.rows, Gm::ACT_ROWS) ||
       !make_map(&m_w0, w0, false, Kdim, (uint64_t)G * N, 128) ||
       !make_map(&m_w1, w1, false, Kdim, (uint64_t)G * N, 128))
@@ -521,7 +563,13 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long n_wt = (N + Gm::W_COLS - 1) / Gm::W_COLS;
   const long long max_tiles = n_wt * ((a.rows + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
-  kern<<<grid, Gm::THREADS, Gm::SMEM, s>>>(m_act, m_w0, m_w1, p);
+  // GEMM-2 tokens-as-M stores y through a tensor map; elsewhere the slot is unused.
+  if (MODE == 1 && !SWAP) {
+    if (!make_map_f32(&m_y, a.y, (uint64_t)N, (uint64_t)a.rows)) return cudaErrorInvalidValue;
+  } else {
+    m_y = m_act;
+  }
+  kern<<<grid, Gm::THREADS, Gm::SMEM, s>>>(m_act, m_w0, m_w1, m_y, p);
   return cudaGetLastError();
 }
 
