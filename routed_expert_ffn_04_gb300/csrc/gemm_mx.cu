@@ -20,13 +20,19 @@
 // A stage's two atoms (A rows, B rows) ride on the same mbarrier as its TMA
 // tiles, and the MMA thread moves them into TMEM with tcgen05.cp.
 //
-// Persistent, one CTA per SM, 192 threads:
+// Persistent, one CTA per SM, 224 threads:
 //   warp 0      producer: per stage, the 128-wide K slice (bytes) of the 128
 //               token rows (A) and 128 weight rows (B) by TMA, plus the two
 //               scale atoms by bulk copy.
-//   warp 1      TMEM allocator + MMA issuer: per stage two tcgen05.cp
-//               (32x128b.warpx4: one 32 x 16-byte atom block replicated into
-//               the four lane quarters) and 4 MMAs (K = 32 each).
+//   warp 6      scale mover: per stage, once the stage has landed, two
+//               tcgen05.cp (32x128b.warpx4: one 32 x 16-byte atom block
+//               replicated into the four lane quarters) into the stage's TMEM
+//               scale slot, committed to the stage's scale barrier.
+//   warp 1      TMEM allocator + MMA issuer: per stage, after the scale
+//               barrier, 4 MMAs (K = 32 each). Each tcgen05 instruction costs
+//               its issuing thread tens of cycles, and at N = 128 the MMA
+//               thread's issue time, not the tensor pipe, sets the pace, so
+//               the copies are issued by another thread.
 //   warps 2..5  epilogue (TMEM -> h codes + scale atoms, or staged fp32 y).
 // Tile: M = 128 tokens, N = 128 (GEMM-1: gate 64 + up 64; GEMM-2: 128 of
 // H), double-buffered fp32 accumulators (256 TMEM columns) plus one 8-column
@@ -48,7 +54,8 @@ namespace {
 
 constexpr int kK = 128;                  // K elements (= bytes) per stage
 constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kMoverWarp = 6;
 constexpr int kTileBytes = 128 * 128;    // 128 rows x 128 bytes
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kSfBytes = 2 * kAtomBytes; // per stage: A atom + B atom
@@ -63,7 +70,7 @@ constexpr int kSmem = 1024 + kStages * kStageBytes + kTableBytes + kBarBytes + k
                       kStages * kSfBytes;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kSfCol0 + 8 * kStages <= kTmemCols, "TMEM budget");
-static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+static_assert((3 * kStages + 6) * 8 + 8 <= kBarBytes, "barrier area");
 static_assert(kTableBytes % 16 == 0 && kEpiBytes % 16 == 0, "scale atoms need 16-byte alignment");
 
 template <int MODE, bool W4>
@@ -86,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* epi_stage = reinterpret_cast<float*>(base + kStages * kStageBytes + kTableBytes + kBarBytes);
   const uint32_t sf_smem0 =
       stage0 + (uint32_t)(kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -94,6 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };  // scales in TMEM
+  const uint32_t sdrain_bar = bar0 + 8u * (3 * kStages + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = (p.N + W_COLS - 1) / W_COLS;
@@ -112,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(sfull_bar(s), 1);
+    mbar_init(sdrain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -213,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
         for (int kb = 0; kb < n_k; ++kb) {
-          if (!mbar_wait_bounded(full_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
+          // The scale barrier completes after the stage's data landed and its
+          // scales reached TMEM.
+          if (!mbar_wait_bounded(sfull_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
                                  p.limit_ns)) {
             ok = false;
             break;
@@ -221,8 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t st = stage0 + rg.s * kStageBytes;
           const uint32_t sf = tmem_base + (uint32_t)(kSfCol0 + 8 * rg.s);
-          tmem_cp_32x128b_warpx4(sf, sf_smem0 + rg.s * kSfBytes);
-          tmem_cp_32x128b_warpx4(sf + 4, sf_smem0 + rg.s * kSfBytes + kAtomBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             umma_mxf8(d, sw128_kmajor_desc(st + k * 32), sw128_kmajor_desc(st + kTileBytes + k * 32),
@@ -238,6 +249,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && issued) {
         umma_commit(drain_bar);
         drain_wait(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else if (warp == kMoverWarp) {
+    // ------------------------------------------------------------ scale mover
+    if (lane == 0) {
+      Ring rg;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        for (int kb = 0; kb < n_k; ++kb) {
+          if (!mbar_wait_bounded(full_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
+                                 p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf = tmem_base + (uint32_t)(kSfCol0 + 8 * rg.s);
+          tmem_cp_32x128b_warpx4(sf, sf_smem0 + rg.s * kSfBytes);
+          tmem_cp_32x128b_warpx4(sf + 4, sf_smem0 + rg.s * kSfBytes + kAtomBytes);
+          issued = true;
+          umma_commit(sfull_bar(rg.s));
+          rg.next(kStages);
+        }
+      }
+      if (!ok && issued) {  // its copies complete before TMEM is freed
+        umma_commit(sdrain_bar);
+        drain_wait(sdrain_bar, 0, 100000000ull);
       }
     }
   } else {
