@@ -511,6 +511,10 @@ bool make_map_f32(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer) {
 
 }  // namespace
 
+bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer) {
+  return make_map_f32(m, ptr, inner, outer);
+}
+
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
   return make_map(m, ptr, true, inner, outer, box_rows);
 }

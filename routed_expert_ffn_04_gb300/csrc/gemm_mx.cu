@@ -65,7 +65,10 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
 constexpr int kTableBytes = (kMaxGroups + 8) * 4;
 constexpr int kBarBytes = 256;
-constexpr int kEpiBytes = 4 * 32 * 33 * 4;
+// Epilogue staging per warp: a 4 KB 128-byte-swizzled block for GEMM-2's bulk
+// stores, or the row-stride-33 layout of its row-by-row path (1024-aligned).
+constexpr int kEpiWarp = 5120;
+constexpr int kEpiBytes = 4 * kEpiWarp;
 constexpr int kSmem = 1024 + kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes +
                       kStages * kSfBytes;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -77,7 +80,8 @@ template <int MODE, bool W4>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap map_act,
                            const __grid_constant__ CUtensorMap map_w0,
-                           const __grid_constant__ CUtensorMap map_w1, const KParams p) {
+                           const __grid_constant__ CUtensorMap map_w1,
+                           const __grid_constant__ CUtensorMap map_y, const KParams p) {
   constexpr int W_COLS = MODE == 0 ? 64 : 128;  // output columns per tile
   // Transaction bytes of a stage: the A tile, the two B boxes (E2M1 boxes count
   // their packed global bytes, half the shared-memory footprint), the atoms.
@@ -88,11 +92,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
   uint8_t* base = smem_raw + pad;
   const uint32_t stage0 = raw_addr + pad;
-  int32_t* tile_start = reinterpret_cast<int32_t*>(base + kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + kTableBytes);
-  float* epi_stage = reinterpret_cast<float*>(base + kStages * kStageBytes + kTableBytes + kBarBytes);
+  // Shared memory: ring | epilogue staging | tile table | barriers | scale atoms.
+  float* epi_stage = reinterpret_cast<float*>(base + kStages * kStageBytes);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(base + kStages * kStageBytes + kEpiBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + kEpiBytes + kTableBytes);
   const uint32_t sf_smem0 =
-      stage0 + (uint32_t)(kStages * kStageBytes + kTableBytes + kBarBytes + kEpiBytes);
+      stage0 + (uint32_t)(kStages * kStageBytes + kEpiBytes + kTableBytes + kBarBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    float* stg = epi_stage + q * 32 * 33;
+    float* stg = epi_stage + q * (kEpiWarp / 4);
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const int acc = local & 1;
@@ -338,7 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // fp32 y, 32 x 32 blocks per warp: one TMA bulk store per block from a
+        // 128-byte-swizzled buffer when all 32 rows belong to the group, row by
+        // row otherwise (a box would also write rows of the next group).
         const int r_first = ti.tt * 128 + q * 32;
+        const bool whole = r_first + 32 <= ti.nrows;
+        const uint32_t stg_u32 = smem_u32(stg);
         float* y = static_cast<float*>(p.out);
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -347,15 +357,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           const int col = ti.wt * 128 + c;
           if (col < p.N) {
+            if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
+            __syncwarp();
+            if (whole) {
+              uint8_t* rowp = reinterpret_cast<uint8_t*>(stg) + lane * 128;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
-            __syncwarp();
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_y, stg_u32, col, ti.row0 + r_first);
+                bulk_commit_group();
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
+              __syncwarp();
 #pragma unroll 4
-            for (int rr = 0; rr < 32; ++rr) {
-              const int row = r_first + rr;
-              if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+              for (int rr = 0; rr < 32; ++rr) {
+                const int row = r_first + rr;
+                if (row < ti.nrows) y[(size_t)(ti.row0 + row) * p.N + col + lane] = stg[rr * 33 + lane];
+              }
+              __syncwarp();
             }
-            __syncwarp();
           }
         }
       }
@@ -363,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's bulk stores are complete
   }
 
   tc_fence_before();
@@ -386,7 +413,7 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   // Whole atoms along K and along the weight rows of a tile.
   if (a.H % 128 || a.I % 128 || a.G > kMaxGroups) return cudaErrorInvalidValue;
   const int G = a.offsets ? a.G : 1;
-  CUtensorMap m_act, m_w0, m_w1;
+  CUtensorMap m_act, m_w0, m_w1, m_y;
   auto wmap = W4 ? make_tmap_e2m1 : make_tmap_u8;
   if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) || !wmap(&m_w0, w0, Kdim, (uint64_t)G * N, 64) ||
       !wmap(&m_w1, w1, Kdim, (uint64_t)G * N, 64))
@@ -407,7 +434,12 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long n_wt = (N + W_COLS - 1) / W_COLS;
   const long long max_tiles = n_wt * ((a.rows + 127) / 128 + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
-  grouped_gemm_mx_kernel<MODE, W4><<<grid, kThreads, kSmem, s>>>(m_act, m_w0, m_w1, p);
+  if (MODE == 1) {  // GEMM-2 stores y blocks through a tensor map
+    if (!make_tmap_f32_store(&m_y, a.y, (uint64_t)N, (uint64_t)a.rows)) return cudaErrorInvalidValue;
+  } else {
+    m_y = m_act;  // unused
+  }
+  grouped_gemm_mx_kernel<MODE, W4><<<grid, kThreads, kSmem, s>>>(m_act, m_w0, m_w1, m_y, p);
   return cudaGetLastError();
 }
 

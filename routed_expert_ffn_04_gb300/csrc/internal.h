@@ -70,6 +70,9 @@ bool gemm_init_driver();  // resolves cuTensorMapEncodeTiled; false if unavailab
 // Opt the GEMM kernels into their dynamic shared memory on the current device
 // (once per device, outside any stream capture).
 cudaError_t gemm_prepare_device();
+// 2-D fp32 tensor map [outer, inner] for bulk stores of 32 x 32 blocks from a
+// 128-byte-swizzled shared-memory buffer (inner % 32 == 0).
+bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer);
 // 2-D uint8 tensor map [outer, inner], box {128 bytes, box_rows}, 128-byte swizzle.
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
 // 2-D packed E2M1 tensor map [outer, inner elements] (inner / 2 bytes per row;
