@@ -32,13 +32,17 @@ sys.path.insert(0, ROOT)
 METRIC = ("MoE-layer tokens/sec at Hy3 shape; achieved HBM GB/s (decode) and TFLOP/s (prefill) vs peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of the routed GEMM-1 kernel (weights-as-M tiling) from the ncu
-# capture summarised in profiles/gemm_gate_up_decode_e48.md:
-# dram__bytes_read.sum + dram__bytes_write.sum = 1.2122 GB + 4.12 MB for 48
-# touched experts, i.e. 25.34 MB per touched expert. It is scaled to a launch
-# by the touched-expert count (each expert's weights stream once), and only
-# reported while gemm.cu is the source the capture was taken on.
-GEMM1_TRAFFIC = {"gemm_cu_sha": "e729a2c2a24a14b9", "bytes_per_touched_expert": (1.2122e9 + 4.12e6) / 48}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
+# GEMM-1 launch in one ncu capture of each full workload at seed 0 (summarised
+# in profiles/gemm1_traffic_full_size.md). A value is reported only while the
+# kernel source still hashes as it did for the capture, and only for the
+# workload as captured (no --experts override).
+GEMM1_TRAFFIC = {
+    "decode": ("gemm.cu", "0c361dcc78bf213a", 4559455744 + 3941120),
+    "prefill": ("gemm.cu", "0c361dcc78bf213a", 5550295296 + 197830400),
+    "mxfp8": ("gemm_mx.cu", "02a99fab6e6d588b", 2565780736 + 27886592),
+    "mxfp4": ("gemm_mx.cu", "02a99fab6e6d588b", 1354861056 + 26868992),
+}
 
 
 def parse():
@@ -218,8 +222,8 @@ def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None
     return n / dt, n, dt, oracle.num_threads()
 
 
-def gemm_cu_sha():
-    p = os.path.join(ROOT, "routed_expert_ffn_04_gb300", "csrc", "gemm.cu")
+def source_sha(name):
+    p = os.path.join(ROOT, "routed_expert_ffn_04_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -305,8 +309,10 @@ def run_ours(args):
         peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         unit = "TFLOP/s"
     traffic = None
-    if GEMM1_TRAFFIC["gemm_cu_sha"] == gemm_cu_sha() and args.workload == "decode":
-        traffic = int(GEMM1_TRAFFIC["bytes_per_touched_expert"] * work["touched"])
+    if args.workload in GEMM1_TRAFFIC and not args.experts:
+        src, sha, nbytes = GEMM1_TRAFFIC[args.workload]
+        if source_sha(src) == sha:
+            traffic = nbytes
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     # route 1, permute 3 + row gather 1, GEMMs 2, shared GEMMs 2, combine 1;
