@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8", "mxfp4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-fold", action="store_true",
+                    help="run the shared expert as one more group of the routed GEMMs (bf16, I_shared == I)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--experts", type=int, default=None,
                     help="override the routed expert count (smaller device footprint for profiler captures)")
@@ -246,6 +248,8 @@ def run_ours(args):
     x, logits = synth.make_activations(shape, device=dev, seed=rank)
     w = synth.make_weights(shape, device=dev, seed=0)
     layer = moe.MoELayer(shape, w, device=local)
+    if args.shared_fold:
+        layer.handle.set_option(moe.MOE_OPT_SHARED_FOLD, 1)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     main = torch.cuda.current_stream(dev)
 
@@ -343,6 +347,8 @@ def run_ours(args):
             "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
             "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "shared_expert": ("one more group of the routed GEMMs" if args.shared_fold and shape.dtype == "bf16"
+                              and shape.I_shared == shape.I else "side stream, event-ordered"),
         },
         "roofline": {
             "kernel": "routed grouped GEMM-1 (gate/up + SwiGLU)",

@@ -119,7 +119,12 @@ typedef enum {
    * moe_read_stage_times can report per-stage device time. Default 0. */
   MOE_OPT_STAGE_TIMING = 1,
   /* Device wait limit in microseconds for bounded spins (default 2000000). */
-  MOE_OPT_WAIT_LIMIT_US = 2
+  MOE_OPT_WAIT_LIMIT_US = 2,
+  /* 1 = run the shared expert as one more group of the routed grouped GEMMs
+   * instead of on the side stream (bf16 layers with I_shared == I and
+   * E <= 1023; otherwise ignored). The result is the same; which is faster
+   * depends on the shape. Default 0 (side stream). */
+  MOE_OPT_SHARED_FOLD = 3
 } moe_option_t;
 
 /* Stage indices reported by moe_read_stage_times. */

@@ -36,6 +36,7 @@ struct moe_handle {
   cudaEvent_t ev_in = nullptr, ev_sh = nullptr;
   int gemm_mode = kModeAuto;
   int stage_timing = 0;
+  int shared_fold = 0;  // MOE_OPT_SHARED_FOLD
   uint64_t wait_limit_ns = kDefaultWaitLimitNs;
   cudaEvent_t* tev = nullptr;  // [kTimingRing][kEventsPerCall], created on first use
   int t_calls = 0;             // calls recorded since the last read
@@ -45,6 +46,8 @@ struct moe_handle {
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__global__ void set_i32_kernel(int32_t* p, int v) { *p = v; }
 
 bool is_mx(int dtype) { return dtype == MOE_MXFP8_E4M3 || dtype == MOE_MXFP4_W4A8; }
 
@@ -73,6 +76,12 @@ moe_status_t check_cfg(const moe_config_t* c) {
   return MOE_OK;
 }
 
+// The shared expert can run as one more group of the routed grouped GEMM
+// (MOE_OPT_SHARED_FOLD): bf16, the same intermediate size, a group to spare.
+bool foldable(const moe_config_t* c) {
+  return c->dtype == MOE_BF16 && c->I_shared > 0 && c->I_shared == c->I && c->E + 1 <= 1024;
+}
+
 // Workspace layout of moe_layer_forward, every piece 256-byte aligned.
 struct Layout {
   size_t topk_idx, topk_w, counts, offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
@@ -94,15 +103,17 @@ Layout layout_of(const moe_config_t* c) {
   L.topk_idx = take(TK * 4);
   L.topk_w = take(TK * 4);
   L.counts = take(E * 4);
-  L.offsets = take((E + 1) * 4);
+  L.offsets = take((E + 2) * 4);  // + the folded shared group's end
   L.perm_src = take(TK * 4);
   L.flat_to_perm = take(TK * 4);
   L.perm_scratch = take(permute_scratch_bytes((int)TK, (int)E));
   const bool mx = is_mx(c->dtype);
   const size_t eb = mx ? 1 : 2;  // bytes per activation element (E4M3 codes or bf16)
-  L.x_perm = take(TK * H * eb);
-  L.h = take(TK * I * eb);
-  L.y_perm = take(TK * H * 4);
+  // Foldable layers keep room for the shared expert's T rows after the routed ones.
+  const size_t RX = TK + (foldable(c) ? T : 0);
+  L.x_perm = take(RX * H * eb);
+  L.h = take(RX * I * eb);
+  L.y_perm = take(RX * H * 4);
   L.s = take(Is ? T * H * 4 : 0);
   L.h_shared = take(T * Is * eb);
   L.x_stage = take(T * H * 2);
@@ -145,6 +156,9 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
   g.s_gate = sg;
   g.s_down = sd;
   g.w4 = 0;
+  g.shared_w_gate = nullptr;
+  g.shared_w_up = nullptr;
+  g.shared_w_down = nullptr;
   g.G = G;
   g.offsets = offsets;
   g.rows = rows;
@@ -272,6 +286,9 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
     case MOE_OPT_WAIT_LIMIT_US:
       if (value <= 0) return MOE_ERR_INVALID_ARG;
       h->wait_limit_ns = (uint64_t)value * 1000ull;
+      return MOE_OK;
+    case MOE_OPT_SHARED_FOLD:
+      h->shared_fold = value ? 1 : 0;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -503,7 +520,7 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     if (timing_events(h) != cudaSuccess) return MOE_ERR_CUDA;
     slot = h->t_calls % kTimingRing;
     ev = h->tev + slot * kEventsPerCall;
-    h->t_shared[slot] = has_shared;
+    h->t_shared[slot] = has_shared && !(h->shared_fold && foldable(cfg));
   }
   auto mark = [&](int i, cudaStream_t s) {
     if (ev) cudaEventRecord(ev[i], s);
@@ -521,7 +538,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     x = xq;
   }
   cudaStream_t s_sh = ss ? ss : sm;
-  if (has_shared) {
+  // Folded: the shared expert is group E of the routed GEMMs (rows TK..TK+T-1
+  // of x_perm, h and y_perm), so nothing runs on the side stream.
+  const bool fold = h->shared_fold && foldable(cfg);
+  if (has_shared && !fold) {
     if (ss) {
       e = cudaEventRecord(h->ev_in, sm);  // input ready on main
       if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, h->ev_in, 0);
@@ -557,11 +577,23 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (e == cudaSuccess && mx)
     e = launch_gather_scale_atoms(xq_s, T, H, perm_src, K, offsets, E, TK,
                                   at<uint8_t>(ws, L.x_perm_s), h->status, sm);
+  if (e == cudaSuccess && fold) {  // group E: x itself, after the routed rows
+    set_i32_kernel<<<1, 1, 0, sm>>>(offsets + E + 1, TK + T);
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(x_perm) + (size_t)TK * H * 2, x, (size_t)T * H * 2,
+                          cudaMemcpyDeviceToDevice, sm);
+  }
   mark(2, sm);
-  GroupedGemmArgs g = gemm_args(h, E, offsets, TK, H, I, x_perm, w->w_gate, w->w_up, w->w_down,
-                                hbuf, y_perm, mx ? w->s_gate : nullptr,
-                                mx ? w->s_down : nullptr);
+  GroupedGemmArgs g = gemm_args(h, fold ? E + 1 : E, offsets, fold ? TK + T : TK, H, I, x_perm,
+                                w->w_gate, w->w_up, w->w_down, hbuf, y_perm,
+                                mx ? w->s_gate : nullptr, mx ? w->s_down : nullptr);
   g.w4 = w4;
+  if (fold) {
+    g.shared_w_gate = w->ws_gate;
+    g.shared_w_up = w->ws_up;
+    g.shared_w_down = w->ws_down;
+  }
   if (mx) {
     g.a_scale = at<uint8_t>(ws, L.x_perm_s);
     g.h_scale = at<uint8_t>(ws, L.h_s);
@@ -570,9 +602,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   mark(3, sm);
   if (e == cudaSuccess) e = mx ? launch_gemm_mx_down(g, sm) : launch_gemm_down(g, sm);
   mark(4, sm);
-  if (e == cudaSuccess && has_shared && ss) e = cudaStreamWaitEvent(sm, h->ev_sh, 0);
+  if (e == cudaSuccess && has_shared && ss && !fold) e = cudaStreamWaitEvent(sm, h->ev_sh, 0);
   if (e == cudaSuccess)
-    e = launch_combine(y_perm, topk_w, flat_to_perm, s_out, T, K, H, out, h->status, sm);
+    e = launch_combine(y_perm, topk_w, flat_to_perm, fold ? y_perm + (size_t)TK * H : s_out, T, K, H,
+                       out, h->status, sm);
   mark(5, sm);
   if (ev) h->t_calls += 1;
   return cuda_status(e);

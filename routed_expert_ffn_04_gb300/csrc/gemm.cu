@@ -22,6 +22,10 @@
 // Tiles are listed per group on the device (no host read of the group sizes)
 // and dealt to CTAs round-robin.
 //
+// Folded shared expert (optional): group p.fold_group takes its weights from a
+// second pair of tensor maps (the shared expert's), so the shared MLP runs as
+// one more group of the routed launch instead of on its own stream.
+//
 // Two tilings (SWAP template flag):
 //   SWAP = true   weights are the 128-row MMA operand A (two A tiles: gate and
 //                 up rows, or two 128-row blocks of W_down) and BN = 32 tokens
@@ -252,7 +256,9 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
                         const __grid_constant__ CUtensorMap map_w0,
                         const __grid_constant__ CUtensorMap map_w1,
-                        const __grid_constant__ CUtensorMap map_y, const KParams p) {
+                        const __grid_constant__ CUtensorMap map_y,
+                        const __grid_constant__ CUtensorMap map_w0s,
+                        const __grid_constant__ CUtensorMap map_w1s, const KParams p) {
   using Gm = Geo<SWAP, MODE, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -304,6 +310,10 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
     prefetch_tensormap(&map_act);
     prefetch_tensormap(&map_w0);
     prefetch_tensormap(&map_w1);
+    if (p.fold_group >= 0) {
+      prefetch_tensormap(&map_w0s);
+      prefetch_tensormap(&map_w1s);
+    }
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the per-group tile counts
@@ -346,7 +356,10 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileInfo ti = decode_tile<Gm::ACT_ROWS>(p, tile_start, tile);
         const int act_row = ti.row0 + ti.tt * Gm::ACT_ROWS;
-        const int w_row0 = ti.g * p.N + ti.wt * Gm::W_COLS;
+        const bool shg = ti.g == p.fold_group;  // the folded shared expert's group
+        const CUtensorMap* mw0 = shg ? &map_w0s : &map_w0;
+        const CUtensorMap* mw1 = shg ? &map_w1s : &map_w1;
+        const int w_row0 = (shg ? 0 : ti.g * p.N) + ti.wt * Gm::W_COLS;
         const int w_row1 = (MODE == 0) ? w_row0 : w_row0 + 128;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
@@ -360,11 +373,11 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
           const uint32_t st = base_u32 + rg.s * Gm::STAGE_BYTES;
           tma_load_2d(st + Gm::ACT_OFF, &map_act, fb, kx, act_row);
           if (SWAP) {
-            tma_load_2d_hint(st + Gm::W_OFF, &map_w0, fb, kx, w_row0, pol_w);
-            tma_load_2d_hint(st + Gm::W_OFF + Gm::kTileBytes, &map_w1, fb, kx, w_row1, pol_w);
+            tma_load_2d_hint(st + Gm::W_OFF, mw0, fb, kx, w_row0, pol_w);
+            tma_load_2d_hint(st + Gm::W_OFF + Gm::kTileBytes, mw1, fb, kx, w_row1, pol_w);
           } else {
-            tma_load_2d(st + Gm::W_OFF, &map_w0, fb, kx, w_row0);
-            tma_load_2d(st + Gm::W_OFF + Gm::kTileBytes, &map_w1, fb, kx, w_row1);
+            tma_load_2d(st + Gm::W_OFF, mw0, fb, kx, w_row0);
+            tma_load_2d(st + Gm::W_OFF + Gm::kTileBytes, mw1, fb, kx, w_row1);
           }
           armed.mark(rg);
           rg.next(NS);
@@ -544,11 +557,24 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const void* w1 = MODE == 0 ? a.w_up : a.w_down;
   if (a.rows == 0 || a.G == 0) return cudaSuccess;
   const int G = a.offsets ? a.G : 1;
-  CUtensorMap m_act, m_w0, m_w1, m_y;
+  // A folded shared expert is the last group; its weights have their own maps.
+  const bool fold = a.shared_w_gate != nullptr && a.offsets != nullptr;
+  const int Gw = fold ? G - 1 : G;  // groups whose weights are in w0 / w1
+  CUtensorMap m_act, m_w0, m_w1, m_y, m_w0s, m_w1s;
   if (!make_map(&m_act, act, false, Kdim, a.rows, Gm::ACT_ROWS) ||
-      !make_map(&m_w0, w0, false, Kdim, (uint64_t)G * N, 128) ||
-      !make_map(&m_w1, w1, false, Kdim, (uint64_t)G * N, 128))
+      !make_map(&m_w0, w0, false, Kdim, (uint64_t)Gw * N, 128) ||
+      !make_map(&m_w1, w1, false, Kdim, (uint64_t)Gw * N, 128))
     return cudaErrorInvalidValue;
+  if (fold) {
+    const void* s0 = MODE == 0 ? a.shared_w_gate : a.shared_w_down;
+    const void* s1 = MODE == 0 ? a.shared_w_up : a.shared_w_down;
+    if (!make_map(&m_w0s, s0, false, Kdim, (uint64_t)N, 128) ||
+        !make_map(&m_w1s, s1, false, Kdim, (uint64_t)N, 128))
+      return cudaErrorInvalidValue;
+  } else {
+    m_w0s = m_w0;  // unused
+    m_w1s = m_w1;
+  }
   auto kern = grouped_gemm_kernel<SWAP, MODE, BN>;
   KParams p = {};
   p.offsets = a.offsets;
@@ -564,6 +590,7 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   p.topk = a.topk;
   p.scaling = a.scaling;
   p.route_norm = a.route_norm;
+  p.fold_group = fold ? G - 1 : -1;
   const long long n_wt = (N + Gm::W_COLS - 1) / Gm::W_COLS;
   const long long max_tiles = n_wt * ((a.rows + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
@@ -573,7 +600,7 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   } else {
     m_y = m_act;
   }
-  kern<<<grid, Gm::THREADS, Gm::SMEM, s>>>(m_act, m_w0, m_w1, m_y, p);
+  kern<<<grid, Gm::THREADS, Gm::SMEM, s>>>(m_act, m_w0, m_w1, m_y, m_w0s, m_w1s, p);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ struct KParams {
   const uint8_t* s_w0;
   const uint8_t* s_act;
   uint8_t* out_scale;
+  // Group that takes the second weight maps (a folded shared expert), or -1.
+  int fold_group;
   // Gating (MODE 2): routing outputs [rows, topk]; `out` (nullable) takes the logits.
   int32_t* topk_idx;
   float* topk_w;

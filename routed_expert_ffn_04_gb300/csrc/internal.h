@@ -62,6 +62,11 @@ struct GroupedGemmArgs {
   const uint8_t* s_gate;
   const uint8_t* s_down;
   int w4;
+  // bf16 only: the shared expert's [I, H], [I, H], [H, I] weights, run as the
+  // last of the G groups (nullptr: every group uses w_gate / w_up / w_down).
+  const void* shared_w_gate;
+  const void* shared_w_up;
+  const void* shared_w_down;
   int num_sms;
   int* status;
   uint64_t wait_limit_ns;

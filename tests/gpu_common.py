@@ -35,15 +35,17 @@ def make_problem(shape, seed=0, device="cpu"):
     return (x.to(dev), logits.to(dev), {k: v.to(dev) for k, v in w.items()})
 
 
-def run_layer(handle, shape, x, logits, w, *, mode=0, side=True, scaling=None, out=None):
+def run_layer(handle, shape, x, logits, w, *, mode=0, side=True, scaling=None, out=None, fold=False):
     cfg = cfg_of(shape, **({} if scaling is None else {"scaling": scaling}))
     handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
+    handle.set_option(moe.MOE_OPT_SHARED_FOLD, int(fold))
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     if out is None:
         out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
     side_stream = torch.cuda.Stream() if side else None
     moe.layer_forward(handle, cfg, moe.make_weights(w), x, logits, out, ws, side=side_stream)
     torch.cuda.synchronize()
+    handle.set_option(moe.MOE_OPT_SHARED_FOLD, 0)
     assert handle.device_status() == 0
     return out
 
