@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or config */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid request the library does not handle */
   MOE_ERR_WORKSPACE = 3,     /* workspace smaller than *_workspace_size */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
   MOE_ERR_DEVICE_TIMEOUT = 5 /* a device-side bounded wait gave up */
