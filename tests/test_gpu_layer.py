@@ -44,6 +44,8 @@ def test_tiny_all_tokens(handle, mode, side):
     synth.MoEShape("noshared", T=50, H=256, E=16, K=4, I=128, I_shared=0),
     synth.MoEShape("one_expert", T=40, H=256, E=1, K=1, I=256, I_shared=0, scaling=1.0),
     synth.MoEShape("wide", T=130, H=512, E=64, K=8, I=256, I_shared=256),
+    # The limits: 1024 experts (1024 groups in the grouped GEMM's tile table), top-32.
+    synth.MoEShape("e1024_k32", T=50, H=128, E=1024, K=32, I=128, I_shared=128),
 ], ids=lambda s: s.name)
 @pytest.mark.parametrize("mode", [1, 2])
 def test_edge_shapes(handle, shape, mode):
