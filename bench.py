@@ -26,6 +26,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -191,35 +193,48 @@ def algorithmic_work(shape, counts):
                 gemm1_flops=4 * H * I * TK)
 
 
-def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None = None):
-    """Time the oracle on a bounded sample of tokens; returns (tokens/s, n, seconds, threads)."""
-    import numpy as np
-
+def oracle_layer_fn(shape, x, logits, w):
+    """The oracle's statement of this workload's layer as f(tokens): bf16, or the
+    MX layer on the oracle's own quantisation of the bf16 weights (W4A8: E2M1
+    routed weights). Conversions happen here, outside any timing."""
     import oracle
 
-    xh = x.cpu()
-    lh = logits.cpu()
-    wh = {k: v.cpu() for k, v in w.items()}
-    args = [wh[k] for k in ("w_gate", "w_up", "w_down")]
-    if shape.I_shared:
-        args += [wh[k] for k in ("ws_gate", "ws_up", "ws_down")]
-    # Convert once, outside the timed calls.
-    import oracle as _o
-    conv = [_o._bf16_bits(a) for a in args]
-    xb = _o._bf16_bits(xh)
+    xb = oracle._bf16_bits(x.cpu())
+    lh = np.ascontiguousarray(logits.cpu().numpy())
+    keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if shape.I_shared else [])
+    if shape.dtype in ("mxfp8", "mxfp4"):
+        w4 = shape.dtype == "mxfp4"
+        mw = {k: (oracle.mxfp4_quantize(w[k].cpu()) if (w4 and k.startswith("w_")) else oracle.mx_quantize(w[k].cpu()))
+              for k in keys}
+
+        def run(toks):
+            oracle.layer_forward_mx(xb, lh, mw, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
+                                    tokens=toks, w4=w4)
+        return run
+    conv = [oracle._bf16_bits(w[k].cpu()) for k in keys]
+
+    def run(toks):
+        oracle.layer_forward(xb, lh, *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
+                             tokens=toks)
+    return run
+
+
+def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None = None):
+    """Time the oracle on a bounded sample of tokens; returns (tokens/s, n, seconds, threads)."""
+    import oracle
+
+    run = oracle_layer_fn(shape, x, logits, w)
     # Calibrate on a small batch (fixed per-call costs amortised), then size the sample.
     n_cal = min(shape.T, 16)
     t0 = time.perf_counter()
-    oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
-                         tokens=np.arange(n_cal, dtype=np.int32))
+    run(np.arange(n_cal, dtype=np.int32))
     t1 = (time.perf_counter() - t0) / n_cal
     n = max(1, int(budget_s / max(t1, 1e-6)))
     if max_tokens is not None:
         n = min(n, max_tokens)
     toks = (np.arange(n) % shape.T).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.layer_forward(xb, lh.numpy(), *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
-                         tokens=toks)
+    run(toks)
     dt = time.perf_counter() - t0
     return n / dt, n, dt, oracle.num_threads()
 
@@ -399,16 +414,11 @@ def run_reference(args):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     x, logits = synth.make_activations(shape, device=dev, seed=0)
     w = synth.make_weights(shape, device=dev, seed=0)
-    keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if shape.I_shared else [])
-    conv = [oracle._bf16_bits(w[k]) for k in keys]
-    xb = oracle._bf16_bits(x)
-    lh = logits.cpu().numpy()
+    run = oracle_layer_fn(shape, x, logits, w)
     del w
 
     def step(n):
-        toks = (np.arange(n) % shape.T).astype(np.int32)
-        oracle.layer_forward(xb, lh, *conv, K=shape.K, scaling=shape.scaling, route_norm=shape.route_norm,
-                             tokens=toks)
+        run((np.arange(n) % shape.T).astype(np.int32))
 
     t0 = time.perf_counter()
     step(1)
@@ -428,7 +438,8 @@ def run_reference(args):
         "impl": "reference",
         "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeds as the CUDA arm)",
+        "vs_baseline": None, "dtype": "f64" + (f" on {shape.dtype} operands" if shape.dtype != "bf16" else ""),
+        "data": "synthetic (same seeds as the CUDA arm)",
         "config": {"workload": f"Hy3-shape {args.workload} MoE layer", "T": shape.T, "H": shape.H, "E": shape.E,
                    "K": shape.K, "I": shape.I, "I_shared": shape.I_shared},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
