@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8", "mxfp4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one CUDA-graph-captured layer call (stage times still come from eager calls)")
+    ap.add_argument("--gated", action="store_true",
+                    help="compute the logits from router weights inside the layer (gating fused with routing)")
     ap.add_argument("--shared-fold", action="store_true",
                     help="run the shared expert as one more group of the routed GEMMs (bf16, I_shared == I)")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -171,7 +175,7 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def algorithmic_work(shape, counts):
+def algorithmic_work(shape, counts, gated=False):
     """Bytes the layer must move and FLOPs it must do, from the expert counts."""
     H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
     touched = int((counts > 0).sum())
@@ -184,8 +188,9 @@ def algorithmic_work(shape, counts):
     wb = 0.5 + 1 / 32 if shape.dtype == "mxfp4" else ab           # routed weights
     w_expert = 3 * H * I * wb
     w_shared = 3 * H * Is * ab
-    layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + T * E * 4 + T * H * 2)
-    flops = 6 * H * I * T * K + 6 * H * Is * T
+    # x, logits (or, gated, the [E, H] bf16 router weights) and out.
+    layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + (E * H * 2 if gated else T * E * 4) + T * H * 2)
+    flops = 6 * H * I * T * K + 6 * H * Is * T + (2 * T * H * E if gated else 0)
     TK = T * K
     # GEMM-1 reads the touched experts' gate/up weights and x_perm, and writes h.
     gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * ab + TK * I * ab)
@@ -272,12 +277,22 @@ def run_ours(args):
     cfg = layer.cfg
     idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device=dev)
     tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device=dev)
-    moe.route(layer.handle, cfg, logits, idx, tw)
+    w_router = synth.make_router(shape, device=dev, seed=0) if args.gated else None
+    if args.gated:
+        moe.gate_route(layer.handle, cfg, x, w_router, idx, tw)
+    else:
+        moe.route(layer.handle, cfg, logits, idx, tw)
     counts = torch.bincount(idx.flatten().long(), minlength=shape.E).cpu().numpy()
-    work = algorithmic_work(shape, counts)
+    work = algorithmic_work(shape, counts, gated=args.gated)
+
+    def call():
+        if args.gated:
+            moe.layer_forward_gated(layer.handle, cfg, layer.weights, w_router, x, out, layer.ws, side=layer.side)
+        else:
+            layer(x, logits, out)
 
     for _ in range(args.warmup):
-        layer(x, logits, out)
+        call()
     torch.cuda.synchronize()
     layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
 
@@ -290,29 +305,64 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(main)
     for _ in range(args.steps):
-        layer(x, logits, out)
+        call()
     ev1.record(main)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = sampler.stop() if sampler else None
-    value, ms = aggregate(shape.T, ev0.elapsed_time(ev1) / args.steps, world, dev)
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
     stage_ms, n_calls = layer.handle.stage_times()
     layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
+    if args.graph:
+        # One captured call (its side-stream fork and join included), replayed.
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(main)
+        with torch.cuda.stream(cap):
+            call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            call()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(main)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        value, ms = aggregate(shape.T, g0.elapsed_time(g1) / args.steps, world, dev)
+    else:
+        value, ms = aggregate(shape.T, eager_ms, world, dev)
+    clocks = sampler.stop() if sampler else None  # sampled over every timed region
     status = layer.handle.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} during the timed region")
 
-    # End-to-end through the host entry point: pinned host x/logits in, out back.
+    # End-to-end through the public API: pinned host x (and logits) in, out back.
     xh = x.cpu().pin_memory()
     lh = logits.cpu().pin_memory()
     oh = torch.empty((shape.T, shape.H), dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def call_host():
+        if args.gated:  # host x -> device, the gated layer, out -> host
+            x.copy_(xh, non_blocking=True)
+            moe.layer_forward_gated(layer.handle, cfg, layer.weights, w_router, x, out, layer.ws, side=layer.side)
+            oh.copy_(out, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+        else:
+            moe.layer_forward_host(layer.handle, cfg, layer.weights, xh, lh, oh, layer.ws, side=layer.side)
+
     for _ in range(3):
-        moe.layer_forward_host(layer.handle, cfg, layer.weights, xh, lh, oh, layer.ws, side=layer.side)
+        call_host()
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        moe.layer_forward_host(layer.handle, cfg, layer.weights, xh, lh, oh, layer.ws, side=layer.side)
+        call_host()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     e2e_ms = dist_max(e2e_ms, world, dev)
 
@@ -362,6 +412,9 @@ def run_ours(args):
             "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
             "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "launch": "CUDA graph replay of one captured layer call" if args.graph else "eager layer calls",
+            "routing_input": ("router weights: gating GEMM with top-k in its epilogue" if args.gated
+                              else "given fp32 logits"),
             "shared_expert": ("one more group of the routed GEMMs" if args.shared_fold and shape.dtype == "bf16"
                               and shape.I_shared == shape.I else "side stream, event-ordered"),
         },
@@ -381,7 +434,7 @@ def run_ours(args):
         },
         "e2e": {"value": round(shape.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": shape.T * shape.H * 2 + shape.T * shape.E * 4,
+                "h2d_bytes_per_step": shape.T * shape.H * 2 + (0 if args.gated else shape.T * shape.E * 4),
                 "d2h_bytes_per_step": shape.T * shape.H * 2},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

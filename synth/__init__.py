@@ -67,7 +67,7 @@ WORKLOADS = {
     "mxfp4": MoEShape("mxfp4", T=2048, H=4096, E=192, K=8, I=1536, I_shared=1536, dtype="mxfp4"),
 }
 
-_STREAMS = dict(x=1, logits=2, bias=3, w_gate=4, w_up=5, w_down=6, ws_gate=7, ws_up=8, ws_down=9)
+_STREAMS = dict(x=1, logits=2, bias=3, w_gate=4, w_up=5, w_down=6, ws_gate=7, ws_up=8, ws_down=9, w_router=10)
 
 
 def _gen(device, seed: int, name: str) -> torch.Generator:
@@ -90,6 +90,12 @@ def make_activations(shape: MoEShape, device="cpu", seed: int = 0):
         bias = _normal((shape.E,), 2.0, torch.float32, device, seed, "bias")
         logits = logits + bias[None, :]
     return x, logits
+
+
+def make_router(shape: MoEShape, device="cpu", seed: int = 0, std: float = 0.02):
+    """Router (gating projection) weights [E, H] bf16 ~ N(0, std), for the layer
+    variant that computes the logits from x instead of taking them."""
+    return _normal((shape.E, shape.H), std, torch.bfloat16, device, seed, "w_router")
 
 
 def make_weights(shape: MoEShape, device="cpu", seed: int = 0, std: float = 0.02):
