@@ -281,9 +281,12 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
                                        moe_stream_t side);
 
 /* Gating + routing ([Hy3] section 8.5: the main stream runs gating, then the
- * routed path): logits = x w_router^T in fp32 (tensor cores, bf16 inputs),
- * then the routing of moe_route. With E <= 256 one kernel does both: the
- * top-k runs in the GEMM epilogue on the fp32 accumulators.
+ * routed path): logits = x w_router^T in fp32 (bf16 inputs), then the
+ * routing of moe_route. With E <= 256 one kernel does both. Up to 512
+ * tokens it is a CUDA-core split-K kernel (a cluster of 8 CTAs per group of
+ * tokens, partial sums added in a fixed order, top-k by one warp per token);
+ * above that a tensor-core GEMM with the top-k in its epilogue on the fp32
+ * accumulators. Either way the result does not depend on logits_out.
  * x (device): [T, H] bf16; w_router (device): [E, H] bf16;
  * logits_out (device, nullable when E <= 256): [T, E] fp32;
  * topk_idx / topk_w (device): [T, K]. E > 256 needs E % 32 == 0. */

@@ -194,6 +194,9 @@ cudaError_t timing_events(moe_handle_t h) {
 // (into `logits`, required then) and runs the routing kernel on them.
 cudaError_t gate_route(moe_handle_t h, const moe_config_t* c, const void* x, const void* w_router,
                        float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+  if (gate_route_small_fits(c->T, c->H, c->E))
+    return launch_gate_route_small(x, w_router, c->T, c->H, c->E, c->K, c->scaling, c->route_norm,
+                                   logits, topk_idx, topk_w, s);
   GroupedGemmArgs g = gemm_args(h, 1, nullptr, c->T, /*H (N)=*/c->E, /*I (K)=*/c->H, x, nullptr,
                                 nullptr, w_router, const_cast<void*>(x), logits);
   if (c->E <= 256) {
@@ -246,6 +249,7 @@ MOE_API moe_status_t moe_create(int device, moe_handle_t* out) {
   h->device = device;
   h->num_sms = sms;
   if (gemm_prepare_device() != cudaSuccess || gemm_mx_prepare_device() != cudaSuccess ||
+      gate_small_prepare_device() != cudaSuccess ||
       cudaMalloc(&h->status, 64) != cudaSuccess ||
       cudaMemset(h->status, 0, 64) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming) != cudaSuccess ||

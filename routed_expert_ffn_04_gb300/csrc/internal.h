@@ -23,6 +23,16 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 cudaError_t launch_route(const float* logits, int T, int E, int K, float scaling, int route_norm,
                          int32_t* topk_idx, float* topk_w, cudaStream_t s);
 
+// ---- gating + routing for few tokens (gate.cu): CUDA-core split-K in one
+// cluster launch, E <= 256, T <= kGateSmallMaxT. x [T, H] and w_router
+// [E, H] bf16; logits [T, E] fp32 out (nullable).
+constexpr int kGateSmallMaxT = 512;
+bool gate_route_small_fits(int T, int H, int E);
+cudaError_t gate_small_prepare_device();
+cudaError_t launch_gate_route_small(const void* x, const void* w_router, int T, int H, int E,
+                                    int K, float scaling, int route_norm, float* logits,
+                                    int32_t* topk_idx, float* topk_w, cudaStream_t s);
+
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int TK, int E);
 cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* scratch,

@@ -3,15 +3,12 @@
 // sigmoid routing over 192 experts; HYV3Config router_scaling_factor=2.826,
 // route_norm=True, moe_router_use_sigmoid=True.
 //
-// One warp per token. Each lane holds ceil(E/32) logits as 64-bit keys:
-//   key = (order-preserving bits of the fp32 logit) << 32 | (0xFFFFFFFF - id)
-// so the largest key is the largest logit and, among equal logits, the lowest
-// id. K rounds of a warp max-reduction pick the experts in slot order; the
-// winning lane clears its key. Key 0 marks an empty / taken slot.
+// One warp per token (route_warp.cuh): each lane holds ceil(E/32) logits as
+// 64-bit keys, K rounds of a warp max-reduction pick the experts in slot order.
 #include <cuda_runtime.h>
 
 #include "internal.h"
-#include "topk_key.cuh"
+#include "route_warp.cuh"
 
 namespace moe {
 namespace {
@@ -21,51 +18,10 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                                                     int K, float scaling, int route_norm,
                                                     int32_t* __restrict__ topk_idx,
                                                     float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* row = logits + (size_t)t * E;
-
-  unsigned long long key[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = j * 32 + lane;
-    key[j] = (e < E) ? make_key(__ldg(row + e), e) : 0ull;
-  }
-
-  int my_id = 0;          // lane k keeps the id of slot k
-  float my_logit = 0.0f;  // and its logit
-  for (int k = 0; k < K; ++k) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-      best = o > best ? o : best;
-    }
-    const int id = key_id(best);
-    if ((id & 31) == lane) {
-#pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (j == (id >> 5)) key[j] = 0ull;
-    }
-    if (lane == k) {
-      my_id = id;
-      my_logit = key_logit(best);
-    }
-  }
-
-  // sigma(l) = 1 / (1 + exp(-l)); route_norm divides by the sum over the K slots.
-  const float sig = (lane < K) ? 1.0f / (1.0f + expf(-my_logit)) : 0.0f;
-  float sum = sig;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-  if (lane < K) {
-    const float w = route_norm ? sig / sum : sig;
-    topk_idx[(size_t)t * K + lane] = my_id;
-    topk_w[(size_t)t * K + lane] = w * scaling;
-  }
+  route_token_warp<VPL>(logits + (size_t)t * E, E, K, scaling, route_norm,
+                        topk_idx + (size_t)t * K, topk_w + (size_t)t * K);
 }
 
 template <int VPL>

@@ -1,8 +1,9 @@
 """GPU checks of the gating projection fused with routing (moe_gate_route)
 and of the layer that routes from it (moe_layer_forward_gated).
 
-The router logits come from bf16 tensor-core products accumulated in fp32,
-while the oracle computes them in fp64, so two experts whose logits lie
+The router logits are bf16 products accumulated in fp32 (split-K on the
+CUDA cores up to 512 tokens, tensor cores above), while the oracle computes
+them in fp64, so two experts whose logits lie
 within rounding of each other may legitimately be ordered either way. The
 tests therefore check:
   - the logits against the oracle (|err| <= 2e-4 + 2e-4 |logit|);
@@ -37,13 +38,24 @@ def _router(shape, seed=11):
     return (torch.randn(shape.E, shape.H, generator=g) * 0.02).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("shape", [
-    synth.WORKLOADS["decode"],
+# Up to 512 tokens (E <= 256) the split-K CUDA-core kernel runs, above that
+# the tensor-core GEMM with the top-k in its epilogue; E > 256 writes the
+# logits and runs the routing kernel.
+GATE_SHAPES = [
+    synth.WORKLOADS["decode"],                                                # split-K, 2 tokens a cluster
+    synth.MoEShape("t1", T=1, H=4096, E=192, K=8, I=256, I_shared=0),         # one token
+    synth.MoEShape("t5_h320", T=5, H=320, E=96, K=4, I=128, I_shared=0),      # K range not a multiple of 16
+    synth.MoEShape("t100", T=100, H=1024, E=192, K=8, I=256, I_shared=0),     # 4 tokens a cluster
+    synth.MoEShape("t512", T=512, H=1024, E=192, K=8, I=256, I_shared=0),     # largest split-K case
+    synth.MoEShape("t513", T=513, H=1024, E=192, K=8, I=256, I_shared=0),     # smallest tensor-core case
     synth.MoEShape("prefill_like", T=1000, H=1024, E=192, K=8, I=256, I_shared=0),
-    synth.MoEShape("e256", T=77, H=512, E=256, K=8, I=128, I_shared=0),
-    synth.MoEShape("e64k1", T=130, H=256, E=64, K=1, I=128, I_shared=0),
-    synth.MoEShape("e512", T=50, H=256, E=512, K=6, I=128, I_shared=0),  # logits + routing kernel path
-], ids=lambda s: s.name)
+    synth.MoEShape("e256", T=77, H=512, E=256, K=8, I=128, I_shared=0),       # ragged last cluster
+    synth.MoEShape("e64k1", T=130, H=256, E=64, K=1, I=128, I_shared=0),      # four K pieces a CTA
+    synth.MoEShape("e512", T=50, H=256, E=512, K=6, I=128, I_shared=0),       # logits + routing kernel path
+]
+
+
+@pytest.mark.parametrize("shape", GATE_SHAPES, ids=lambda s: s.name)
 def test_gate_route(handle, shape):
     x, _ = synth.make_activations(shape, device="cuda", seed=3)
     wr = _router(shape).cuda()
@@ -72,8 +84,8 @@ def test_gate_route(handle, shape):
     assert all(len(set(r)) == shape.K for r in ids.tolist())
 
 
-def test_gate_route_without_logits_output(handle):
-    shape = synth.WORKLOADS["decode"]
+@pytest.mark.parametrize("shape", [synth.WORKLOADS["decode"], GATE_SHAPES[5]], ids=lambda s: s.name)
+def test_gate_route_without_logits_output(handle, shape):
     x, _ = synth.make_activations(shape, device="cuda", seed=4)
     wr = _router(shape).cuda()
     cfg = cfg_of(shape)
@@ -86,7 +98,10 @@ def test_gate_route_without_logits_output(handle):
     assert torch.equal(idx, idx2) and torch.equal(w, w2)
 
 
-@pytest.mark.parametrize("shape", [synth.WORKLOADS["tiny"], synth.WORKLOADS["decode"]], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [
+    synth.WORKLOADS["tiny"], synth.WORKLOADS["decode"],
+    synth.MoEShape("t600", T=600, H=512, E=64, K=4, I=128, I_shared=128),  # tensor-core gating
+], ids=lambda s: s.name)
 def test_gated_layer_matches_oracle(handle, shape):
     x, _ = synth.make_activations(shape, device="cuda", seed=5)
     w = synth.make_weights(shape, device="cuda", seed=5)
