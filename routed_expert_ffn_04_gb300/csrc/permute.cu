@@ -13,6 +13,9 @@
 //   3. scatter: each warp walks its chunk in flat order, 32 at a time; lanes
 //               with equal ids are grouped with __match_any_sync and ranked
 //               by lane order, so rows of one expert keep ascending f.
+// Up to kSmallMaxTK pairs the three run as the phases of one 1024-thread
+// block (perm_small_kernel), with the per-warp counters in shared memory: the
+// same counting sort, one launch instead of three.
 // A fourth kernel gathers rows with 16-byte vector copies.
 #include <cuda_runtime.h>
 
@@ -149,6 +152,102 @@ __global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
   }
 }
 
+// Counting sort of up to kSmallMaxTK pairs by one block: warp w (w < NW) owns
+// flat indices [w*chunk, (w+1)*chunk). Phase 1 counts them per expert into
+// hist[w][e]; phase 2 turns the counts into exclusive bases (warps in order
+// within an expert, experts in order) and writes counts / offsets; phase 3
+// ranks equal ids within each 32-index step with __match_any_sync, as
+// perm_scatter_kernel does, so rows of one expert keep ascending f.
+constexpr int kSmallMaxTK = 8192;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallHistInts = 12224;  // counters (NW * E <= this) + 128 B static < 48 KB
+
+__global__ void __launch_bounds__(kSmallThreads) perm_small_kernel(
+    const int32_t* __restrict__ idx, int TK, int E, int NW, int chunk,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ flat_to_perm, int* status) {
+  extern __shared__ int32_t hist[];  // [NW][E]
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < NW * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+
+  if (warp < NW) {
+    int32_t* h = hist + warp * E;
+    for (int p = 0; p < chunk; p += 32) {
+      const int f = warp * chunk + p + lane;
+      if (f < TK) {
+        const int e = __ldg(idx + f);
+        if ((unsigned)e < (unsigned)E) atomicAdd(h + e, 1);
+        else atomicCAS(status, 0, MOE_DEV_BAD_EXPERT_ID);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Thread e: bases of expert e relative to its start, and its total.
+  int32_t v = 0;
+  if (tid < E)
+    for (int w = 0; w < NW; ++w) {
+      const int32_t c = hist[w * E + tid];
+      hist[w * E + tid] = v;
+      v += c;
+    }
+  // Block exclusive scan of the totals (E <= 1024 = one entry per thread).
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t wv = warp_tot[lane];
+    int32_t winc = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, winc, off);
+      if (lane >= off) winc += u;
+    }
+    warp_tot[lane] = winc - wv;
+  }
+  __syncthreads();
+  const int32_t excl = warp_tot[warp] + incl - v;
+  if (tid < E) {
+    offsets[tid] = excl;
+    counts[tid] = v;
+    if (tid == E - 1) offsets[E] = excl + v;
+    for (int w = 0; w < NW; ++w) hist[w * E + tid] += excl;
+  }
+  __syncthreads();
+
+  if (warp < NW) {
+    int32_t* run = hist + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int p = 0; p < chunk; p += 32) {
+      const int f = warp * chunk + p + lane;
+      int e = -1;
+      if (f < TK) {
+        e = __ldg(idx + f);
+        if ((unsigned)e >= (unsigned)E) e = -1;
+      }
+      const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+      const int rank = __popc(same & lt_mask);
+      const int leader = __ffs(same) - 1;
+      int pos = 0;
+      if (e >= 0) pos = run[e] + rank;
+      __syncwarp();
+      if (e >= 0 && lane == leader) run[e] += __popc(same);
+      __syncwarp();
+      if (e >= 0) {
+        perm_src[pos] = f;
+        flat_to_perm[f] = pos;
+      }
+    }
+  }
+}
+
 // One warp per destination row; each lane copies vectors (16 bytes, or 4
 // for short rows such as MX scale rows), four in flight.
 template <typename V>
@@ -192,6 +291,15 @@ size_t permute_scratch_bytes(int TK, int E) {
 cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* scratch,
                                  int32_t* counts, int32_t* offsets, int32_t* perm_src,
                                  int32_t* flat_to_perm, int* status, cudaStream_t s) {
+  if (TK > 0 && TK <= kSmallMaxTK) {
+    int nw = (TK + 31) / 32;
+    if (nw > 32) nw = 32;
+    if (nw > kSmallHistInts / E) nw = kSmallHistInts / E;
+    const int chunk = ((TK + nw - 1) / nw + 31) / 32 * 32;
+    perm_small_kernel<<<1, kSmallThreads, (size_t)nw * E * sizeof(int32_t), s>>>(
+        topk_idx, TK, E, nw, chunk, counts, offsets, perm_src, flat_to_perm, status);
+    return cudaGetLastError();
+  }
   const int NW = (TK + kChunk - 1) / kChunk;
   int32_t* hist = static_cast<int32_t*>(scratch);
   const size_t smem = (size_t)kWarps * E * sizeof(int32_t);
