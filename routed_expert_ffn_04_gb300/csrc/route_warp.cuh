@@ -41,11 +41,9 @@ __device__ __forceinline__ void route_token_warp(const float* row, int E, int K,
       best = o > best ? o : best;
     }
     const int id = key_id(best);
-    if ((id & 31) == lane) {
+    const bool mine = (id & 31) == lane;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (j == (id >> 5)) key[j] = 0ull;
-    }
+    for (int j = 0; j < VPL; ++j) key[j] = (mine && j == (id >> 5)) ? 0ull : key[j];
     if (lane == k) {
       my_id = id;
       my_logit = key_logit(best);
