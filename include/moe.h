@@ -282,7 +282,7 @@ MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
 
 /* Gating + routing ([Hy3] section 8.5: the main stream runs gating, then the
  * routed path): logits = x w_router^T in fp32 (bf16 inputs), then the
- * routing of moe_route. With E <= 256 one kernel does both. Up to 512
+ * routing of moe_route. With E <= 256 one kernel does both. Up to 256
  * tokens it is a CUDA-core split-K kernel (a cluster of 8 CTAs per group of
  * tokens, partial sums added in a fixed order, top-k by one warp per token);
  * above that a tensor-core GEMM with the top-k in its epilogue on the fp32

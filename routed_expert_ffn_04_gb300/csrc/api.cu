@@ -542,6 +542,14 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     x = xq;
   }
   cudaStream_t s_sh = ss ? ss : sm;
+  // Gated: the gating projection and the routing run first, and the side
+  // stream forks after them ([Hy3] section 8.5: gating, then the shared
+  // expert beside the routed path), so the gating kernel does not queue
+  // behind the shared expert's persistent GEMMs for SMs.
+  if (e == cudaSuccess && w_router) {
+    e = gate_route(h, cfg, x_gate, w_router, at<float>(ws, L.logits_stage), topk_idx, topk_w, sm);
+    mark(1, sm);
+  }
   // Folded: the shared expert is group E of the routed GEMMs (rows TK..TK+T-1
   // of x_perm, h and y_perm), so nothing runs on the side stream.
   const bool fold = h->shared_fold && foldable(cfg);
@@ -566,13 +574,11 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     mark(7, s_sh);
     if (e == cudaSuccess && ss) e = cudaEventRecord(h->ev_sh, ss);  // shared MLP done
   }
-  if (e == cudaSuccess) {
-    if (w_router)
-      e = gate_route(h, cfg, x_gate, w_router, at<float>(ws, L.logits_stage), topk_idx, topk_w, sm);
-    else
+  if (!w_router) {
+    if (e == cudaSuccess)
       e = launch_route(logits, T, E, K, cfg->scaling, cfg->route_norm, topk_idx, topk_w, sm);
+    mark(1, sm);
   }
-  mark(1, sm);
   if (e == cudaSuccess)
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
                              perm_src, flat_to_perm, h->status, sm);

@@ -54,6 +54,7 @@ namespace {
 
 constexpr int kBK = 64;            // K elements per stage = one 128-byte swizzle row of bf16
 constexpr int kMaxGroups = 1024;
+constexpr int kTopSlots = 8;       // gating epilogue: top-k kept in registers up to this K
 constexpr int kMaxSmem = 232448;   // 227 KB dynamic shared memory per CTA
 
 template <bool SWAP, int MODE, int BN>
@@ -164,43 +165,94 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
       }
     } else if (MODE == 2) {
       // Fused routing of this token: its E logits sit in TMEM columns 0..E-1.
-      // Round k takes the largest key below the previous pick (keys are
-      // unique), so no list of taken experts is kept.
       const int E = p.N;
-      float* lrow = static_cast<float*>(p.out);
-      if (lrow) lrow += (size_t)(ti.row0 + (rv ? r : 0)) * E;
+      const int rbase = ti.row0 + ti.tt * 128 + q * 32;  // this warp's first row
+      const int nvalid = ti.nrows - (ti.tt * 128 + q * 32);
+      float* lout = static_cast<float*>(p.out);
       const size_t orow = (size_t)(ti.row0 + (rv ? r : 0)) * p.topk;
-      unsigned long long prev = ~0ull;
-      float sum = 0.0f;
-#pragma unroll 1
-      for (int k = 0; k < p.topk; ++k) {
-        unsigned long long best = 0ull;
+      if (p.topk <= kTopSlots) {
+        // One pass over the logits with the best kTopSlots keys kept sorted
+        // in registers (keys are unique, so the order is strict). The logits,
+        // when asked for, leave through the warp's 32 x 33 staging block so
+        // that each store instruction writes one row's 32 consecutive floats.
+        unsigned long long top[kTopSlots];
+#pragma unroll
+        for (int j = 0; j < kTopSlots; ++j) top[j] = 0ull;
 #pragma unroll 1
         for (int c = 0; c < E; c += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tb + c, v);
           tmem_ld_wait();
+          if (lout) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[lane * 33 + j] = __uint_as_float(v[j]);
+            __syncwarp();
+            const int nr = nvalid < 32 ? nvalid : 32;
+            for (int rr = 0; rr < nr; ++rr)
+              if (c + lane < E) lout[(size_t)(rbase + rr) * E + c + lane] = stg[rr * 33 + lane];
+            __syncwarp();
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int e = c + j;
-            const float l = __uint_as_float(v[j]);
-            if (k == 0 && lrow && rv && e < E) lrow[e] = l;
-            const unsigned long long key = e < E ? make_key(l, e) : 0ull;
-            if (key < prev && key > best) best = key;
+            const unsigned long long key =
+                c + j < E ? make_key(__uint_as_float(v[j]), c + j) : 0ull;
+#pragma unroll
+            for (int s = kTopSlots - 1; s > 0; --s)
+              top[s] = key > top[s - 1] ? top[s - 1] : (key > top[s] ? key : top[s]);
+            top[0] = key > top[0] ? key : top[0];
           }
         }
-        prev = best;
-        const float sig = 1.0f / (1.0f + expf(-key_logit(best)));
-        sum += sig;
-        if (rv) {
-          p.topk_idx[orow + k] = key_id(best);
-          p.topk_w[orow + k] = sig;
+        float sig[kTopSlots];
+        float sum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kTopSlots; ++k) {
+          sig[k] = 1.0f / (1.0f + expf(-key_logit(top[k])));
+          if (k < p.topk) sum += sig[k];
         }
-      }
-      if (rv) {
+        if (rv) {
+#pragma unroll
+          for (int k = 0; k < kTopSlots; ++k)
+            if (k < p.topk) {
+              p.topk_idx[orow + k] = key_id(top[k]);
+              p.topk_w[orow + k] = (p.route_norm ? sig[k] / sum : sig[k]) * p.scaling;
+            }
+        }
+      } else {
+        // K > kTopSlots: K rounds, each taking the largest key below the
+        // previous pick, so no list of taken experts is kept.
+        float* lrow = lout ? lout + (size_t)(ti.row0 + (rv ? r : 0)) * E : nullptr;
+        unsigned long long prev = ~0ull;
+        float sum = 0.0f;
+#pragma unroll 1
         for (int k = 0; k < p.topk; ++k) {
-          const float sig = p.topk_w[orow + k];
-          p.topk_w[orow + k] = (p.route_norm ? sig / sum : sig) * p.scaling;
+          unsigned long long best = 0ull;
+#pragma unroll 1
+          for (int c = 0; c < E; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tb + c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int e = c + j;
+              const float l = __uint_as_float(v[j]);
+              if (k == 0 && lrow && rv && e < E) lrow[e] = l;
+              const unsigned long long key = e < E ? make_key(l, e) : 0ull;
+              if (key < prev && key > best) best = key;
+            }
+          }
+          prev = best;
+          const float sig = 1.0f / (1.0f + expf(-key_logit(best)));
+          sum += sig;
+          if (rv) {
+            p.topk_idx[orow + k] = key_id(best);
+            p.topk_w[orow + k] = sig;
+          }
+        }
+        if (rv) {
+          for (int k = 0; k < p.topk; ++k) {
+            const float sig = p.topk_w[orow + k];
+            p.topk_w[orow + k] = (p.route_norm ? sig / sum : sig) * p.scaling;
+          }
         }
       }
     } else {

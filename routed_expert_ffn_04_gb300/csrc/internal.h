@@ -26,7 +26,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, float scaling
 // ---- gating + routing for few tokens (gate.cu): CUDA-core split-K in one
 // cluster launch, E <= 256, T <= kGateSmallMaxT. x [T, H] and w_router
 // [E, H] bf16; logits [T, E] fp32 out (nullable).
-constexpr int kGateSmallMaxT = 512;
+constexpr int kGateSmallMaxT = 256;
 bool gate_route_small_fits(int T, int H, int E);
 cudaError_t gate_small_prepare_device();
 cudaError_t launch_gate_route_small(const void* x, const void* w_router, int T, int H, int E,

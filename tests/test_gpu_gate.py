@@ -2,7 +2,7 @@
 and of the layer that routes from it (moe_layer_forward_gated).
 
 The router logits are bf16 products accumulated in fp32 (split-K on the
-CUDA cores up to 512 tokens, tensor cores above), while the oracle computes
+CUDA cores up to 256 tokens, tensor cores above), while the oracle computes
 them in fp64, so two experts whose logits lie
 within rounding of each other may legitimately be ordered either way. The
 tests therefore check:
@@ -38,7 +38,7 @@ def _router(shape, seed=11):
     return (torch.randn(shape.E, shape.H, generator=g) * 0.02).to(torch.bfloat16)
 
 
-# Up to 512 tokens (E <= 256) the split-K CUDA-core kernel runs, above that
+# Up to 256 tokens (E <= 256) the split-K CUDA-core kernel runs, above that
 # the tensor-core GEMM with the top-k in its epilogue; E > 256 writes the
 # logits and runs the routing kernel.
 GATE_SHAPES = [
@@ -46,8 +46,9 @@ GATE_SHAPES = [
     synth.MoEShape("t1", T=1, H=4096, E=192, K=8, I=256, I_shared=0),         # one token
     synth.MoEShape("t5_h320", T=5, H=320, E=96, K=4, I=128, I_shared=0),      # K range not a multiple of 16
     synth.MoEShape("t100", T=100, H=1024, E=192, K=8, I=256, I_shared=0),     # 4 tokens a cluster
-    synth.MoEShape("t512", T=512, H=1024, E=192, K=8, I=256, I_shared=0),     # largest split-K case
-    synth.MoEShape("t513", T=513, H=1024, E=192, K=8, I=256, I_shared=0),     # smallest tensor-core case
+    synth.MoEShape("t256", T=256, H=1024, E=192, K=8, I=256, I_shared=0),     # largest split-K case
+    synth.MoEShape("t257", T=257, H=1024, E=192, K=8, I=256, I_shared=0),     # smallest tensor-core case
+    synth.MoEShape("t700_k12", T=700, H=512, E=96, K=12, I=256, I_shared=0),  # K > 8: K-round epilogue
     synth.MoEShape("prefill_like", T=1000, H=1024, E=192, K=8, I=256, I_shared=0),
     synth.MoEShape("e256", T=77, H=512, E=256, K=8, I=128, I_shared=0),       # ragged last cluster
     synth.MoEShape("e64k1", T=130, H=256, E=64, K=1, I=128, I_shared=0),      # four K pieces a CTA
