@@ -55,8 +55,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8", "mxfp4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--graph", action="store_true",
-                    help="time replays of one CUDA-graph-captured layer call (stage times still come from eager calls)")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager layer calls; by default one captured call is replayed as a CUDA graph")
+    ap.add_argument("--graph", action="store_true", help="(the default) time CUDA-graph replays")
     ap.add_argument("--gated", action="store_true",
                     help="compute the logits from router weights inside the layer (gating fused with routing)")
     ap.add_argument("--shared-fold", action="store_true",
@@ -250,6 +251,35 @@ def source_sha(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def time_graph(call, args, main, dev, world):
+    """Capture one layer call (its side-stream fork and join included) as a
+    CUDA graph and return the mean milliseconds of `args.steps` replays,
+    between barriers and device synchronisations."""
+    import torch
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(main)
+    with torch.cuda.stream(cap):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        call()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(main)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(main)
+    torch.cuda.synchronize()
+    barrier(world)
+    return g0.elapsed_time(g1) / args.steps
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -312,31 +342,15 @@ def run_ours(args):
     eager_ms = ev0.elapsed_time(ev1) / args.steps
     stage_ms, n_calls = layer.handle.stage_times()
     layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
-    if args.graph:
-        # One captured call (its side-stream fork and join included), replayed.
-        cap = torch.cuda.Stream(device=dev)
-        cap.wait_stream(main)
-        with torch.cuda.stream(cap):
-            call()
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            call()
-        torch.cuda.synchronize()
-        for _ in range(args.warmup):
-            graph.replay()
-        torch.cuda.synchronize()
-        barrier(world)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(main)
-        for _ in range(args.steps):
-            graph.replay()
-        g1.record(main)
-        torch.cuda.synchronize()
-        barrier(world)
-        value, ms = aggregate(shape.T, g0.elapsed_time(g1) / args.steps, world, dev)
-    else:
-        value, ms = aggregate(shape.T, eager_ms, world, dev)
+    launch = "eager layer calls"
+    graph_ms = None
+    if not args.eager:
+        try:
+            graph_ms = time_graph(call, args, main, dev, world)
+            launch = "CUDA graph replay of one captured layer call"
+        except RuntimeError as exc:  # keep the eager number, say why
+            launch = f"eager layer calls (graph capture failed: {str(exc).splitlines()[0][:120]})"
+    value, ms = aggregate(shape.T, graph_ms if graph_ms is not None else eager_ms, world, dev)
     clocks = sampler.stop() if sampler else None  # sampled over every timed region
     status = layer.handle.device_status()
     if status != 0:
@@ -417,8 +431,9 @@ def run_ours(args):
             "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
             "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": "CUDA graph replay of one captured layer call" if args.graph else "eager layer calls",
-            "routing_input": ("router weights: gating GEMM with top-k in its epilogue" if args.gated
+            "launch": launch,
+            "eager_ms_per_step": round(eager_ms, 5),
+            "routing_input": ("router weights: gating kernel with the top-k fused in" if args.gated
                               else "given fp32 logits"),
             "shared_expert": ("one more group of the routed GEMMs" if args.shared_fold and shape.dtype == "bf16"
                               and shape.I_shared == shape.I else "side stream, event-ordered"),
