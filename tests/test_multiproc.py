@@ -49,3 +49,34 @@ def test_single_rank_needs_no_process_group():
 
     value, ms = bench.aggregate(64, 1.25, 1, torch.device("cpu"))
     assert ms == 1.25 and value == pytest.approx(64 / 1.25e-3)
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    # The reference arm is the oracle on the host cores: it runs without a GPU.
+    (line,) = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+                      {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
