@@ -398,12 +398,12 @@ def run_ours(args):
             traffic = nbytes
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
-    # route 1; permute 1 (one block up to 8192 pairs, else 3) + row gather 1;
+    # route 1; permute 1 (one block up to 16384 pairs, else 3) + row gather 1;
     # GEMMs 2; shared GEMMs 2 (folded: one small kernel that sets the extra
     # group's end); combine 1. MX adds the quantiser of x and the gather of
     # its scale atoms.
     tk = shape.T * shape.K
-    permute_launches = (1 if tk <= 8192 else 3) + 1
+    permute_launches = (1 if tk <= 16384 else 3) + 1
     shared_launches = (1 if args.shared_fold and shape.dtype == "bf16" else 2) if shape.I_shared else 0
     launches_per_step = 1 + permute_launches + 2 + shared_launches + 1 + (2 if shape.dtype != "bf16" else 0)
 

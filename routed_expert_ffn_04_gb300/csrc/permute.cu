@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
 // within an expert, experts in order) and writes counts / offsets; phase 3
 // ranks equal ids within each 32-index step with __match_any_sync, as
 // perm_scatter_kernel does, so rows of one expert keep ascending f.
-constexpr int kSmallMaxTK = 8192;
+constexpr int kSmallMaxTK = 16384;
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallHistInts = 12224;  // counters (NW * E <= this) + 128 B static < 48 KB
 

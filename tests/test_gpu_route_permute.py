@@ -96,9 +96,9 @@ PERM_CASES = {
     "ragged": synth.MoEShape("ragged", T=77, H=128, E=13, K=3, I=64, I_shared=0),
     "e1024": synth.MoEShape("e1024", T=300, H=64, E=1024, K=32, I=64, I_shared=0),
     "t1": synth.MoEShape("t1", T=1, H=64, E=8, K=2, I=64, I_shared=0),
-    # one-block counting sort up to 8192 pairs, three kernels above
-    "tk8192": synth.MoEShape("tk8192", T=1024, H=64, E=192, K=8, I=64, I_shared=0),
-    "tk8200": synth.MoEShape("tk8200", T=1025, H=64, E=192, K=8, I=64, I_shared=0),
+    # one-block counting sort up to 16384 pairs, three kernels above
+    "tk16384": synth.MoEShape("tk16384", T=2048, H=64, E=192, K=8, I=64, I_shared=0),
+    "tk16392": synth.MoEShape("tk16392", T=2049, H=64, E=192, K=8, I=64, I_shared=0),
     "e1024_one_block": synth.MoEShape("e1024s", T=200, H=64, E=1024, K=32, I=64, I_shared=0),
 }
 
