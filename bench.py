@@ -380,6 +380,36 @@ def run_ours(args):
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     e2e_ms = dist_max(e2e_ms, world, dev)
 
+    # How much of the shared expert the second stream hides (the two-stream
+    # timeline check): the same eager calls with the shared expert serial on
+    # the main stream, where its stage is the shared MLP alone.
+    overlap = None
+    if shape.I_shared and not (args.shared_fold and shape.dtype == "bf16"):
+        def call_serial():
+            if args.gated:
+                moe.layer_forward_gated(layer.handle, cfg, layer.weights, w_router, x, out, layer.ws, side=None)
+            else:
+                moe.layer_forward(layer.handle, cfg, layer.weights, x, logits, out, layer.ws, side=None)
+
+        n_ov = max(3, min(args.steps, 200))
+        for _ in range(3):
+            call_serial()
+        torch.cuda.synchronize()
+        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(main)
+        for _ in range(n_ov):
+            call_serial()
+        s1.record(main)
+        torch.cuda.synchronize()
+        serial_ms = s0.elapsed_time(s1) / n_ov
+        st_serial, _ = layer.handle.stage_times()
+        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
+        shared_alone = st_serial["shared"]
+        overlap = {"two_stream_ms": round(eager_ms, 5), "serial_ms": round(serial_ms, 5),
+                   "shared_alone_ms": round(shared_alone, 5),
+                   "hidden_fraction": round((serial_ms - eager_ms) / shared_alone, 3) if shared_alone > 0 else None}
+
     peaks, peak_src = load_peaks()
     g1_ms = stage_ms["gemm_gate_up"]
     bound = "hbm" if args.workload in ("decode", "tiny", "mxfp8", "mxfp4") else "tensor"
@@ -458,6 +488,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": shape.T * shape.H * 2},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "shared_overlap": overlap,
     }
     if rank == 0 and not args.no_cpu_baseline:
         rate, n, dt, thr = cpu_oracle_rate(shape, x, logits, w, budget_s=12.0)
