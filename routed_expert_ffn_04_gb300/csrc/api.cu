@@ -562,6 +562,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     GroupedGemmArgs g = gemm_args(h, 1, nullptr, T, H, Is, x, w->ws_gate, w->ws_up, w->ws_down,
                                   h_shared, s_out, mx ? w->ss_gate : nullptr,
                                   mx ? w->ss_down : nullptr);
+    // Beside the routed path the shared MLP should finish early rather than
+    // use few SMs well: up to 128 tokens its weights fill the MMA rows
+    // (more CTAs stream them) unless a tiling is forced.
+    if (!mx && g.mode == kModeAuto && T <= 128) g.mode = kModeWeightsM;
     if (mx) {
       g.a_scale = at<uint8_t>(ws, L.x_mx_atoms);
       g.h_scale = at<uint8_t>(ws, L.h_shared_s);
