@@ -125,3 +125,34 @@ def test_gated_layer_matches_oracle(handle, shape):
     same = np.all(np.sort(idx.cpu().numpy(), 1) == np.sort(ridx, 1), axis=1)
     assert same.mean() > 0.9
     check_layer(out, ref[same], rows=np.nonzero(same)[0], what=f"gated {shape.name}")
+
+
+@pytest.mark.parametrize("dtype", ["mxfp8", "mxfp4"])
+def test_gated_mx_layer_matches_oracle(handle, dtype):
+    # The router reads the bf16 x also in MX mode; the layer then quantises x
+    # and runs the MX path on the routing the gating kernel chose.
+    shape = synth.WORKLOADS["tiny"].with_(dtype=dtype, T=40)
+    x, _ = synth.make_activations(shape, device="cuda", seed=6)
+    w = synth.make_weights(shape, device="cuda", seed=6)
+    wr = _router(shape, seed=13).cuda()
+    layer = moe.MoELayer(shape, w, device=0)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+    moe.layer_forward_gated(layer.handle, layer.cfg, layer.weights, wr, x, out, layer.ws, side=layer.side)
+    torch.cuda.synchronize()
+    assert layer.handle.device_status() == 0
+    ref_logits = oracle.gate(x.cpu(), wr.cpu()).astype(np.float32)
+    w4 = dtype == "mxfp4"
+    mx_w = {k: (oracle.mxfp4_quantize(v.cpu()) if (w4 and k.startswith("w_")) else oracle.mx_quantize(v.cpu()))
+            for k, v in w.items()}
+    ref = oracle.layer_forward_mx(x.cpu(), ref_logits, mx_w, K=shape.K, scaling=shape.scaling, w4=w4)
+    ridx, _ = oracle.route(ref_logits, shape.K, shape.scaling)
+    idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device="cuda")
+    tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device="cuda")
+    moe.gate_route(layer.handle, layer.cfg, x, wr, idx, tw)
+    torch.cuda.synchronize()
+    same = np.all(np.sort(idx.cpu().numpy(), 1) == np.sort(ridx, 1), axis=1)
+    assert same.mean() > 0.9
+    got = out.float().cpu().numpy().astype(np.float64)[same]
+    r = ref[same]
+    rel = np.linalg.norm(got - r) / np.linalg.norm(r)
+    assert np.all(np.isfinite(got)) and rel <= 3e-2 and np.abs(got - r).max() <= 2e-2, (rel, np.abs(got - r).max())
