@@ -52,3 +52,32 @@ def test_captured_layer_replays_like_eager(dtype, gated):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), seed
     assert handle.device_status() == 0
+
+
+def test_full_decode_workload_replays_like_eager():
+    # The bench times graph replays of the full decode workload; eager calls
+    # of that workload are checked against the oracle in test_gpu_layer.py.
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    moe.load(build_if_missing=True)
+    shape = synth.WORKLOADS["decode"]
+    layer = moe.MoELayer(shape, synth.make_weights(shape, device="cuda", seed=0), device=0)
+    x, logits = synth.make_activations(shape, device="cuda", seed=0)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+    ref = torch.empty_like(out)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        layer(x, logits, out, main=cap)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        layer(x, logits, out, main=cap)
+    torch.cuda.synchronize()
+    layer(x, logits, ref)
+    torch.cuda.synchronize()
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert layer.handle.device_status() == 0
