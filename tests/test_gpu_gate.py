@@ -20,7 +20,7 @@ import torch
 import oracle
 import routed_expert_ffn_04_gb300 as moe
 import synth
-from gpu_common import check_layer, cfg_of
+from gpu_common import check_layer, cfg_of, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -156,3 +156,30 @@ def test_gated_mx_layer_matches_oracle(handle, dtype):
     r = ref[same]
     rel = np.linalg.norm(got - r) / np.linalg.norm(r)
     assert np.all(np.isfinite(got)) and rel <= 3e-2 and np.abs(got - r).max() <= 2e-2, (rel, np.abs(got - r).max())
+
+
+def test_gated_full_prefill_sampled(handle):
+    # The bench's gated prefill line: T = 8192 takes the tcgen05 gating path.
+    shape = synth.WORKLOADS["prefill"]
+    x, _ = synth.make_activations(shape, device="cuda", seed=0)
+    w = synth.make_weights(shape, device="cuda", seed=0)
+    wr = synth.make_router(shape, device="cuda", seed=0)
+    layer = moe.MoELayer(shape, w, device=0)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+    moe.layer_forward_gated(layer.handle, layer.cfg, layer.weights, wr, x, out, layer.ws, side=layer.side)
+    idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device="cuda")
+    tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device="cuda")
+    moe.gate_route(layer.handle, layer.cfg, x, wr, idx, tw)
+    torch.cuda.synchronize()
+    assert layer.handle.device_status() == 0
+    ref_logits = oracle.gate(x.cpu(), wr.cpu()).astype(np.float32)
+    ridx, _ = oracle.route(ref_logits, shape.K, shape.scaling)
+    tokens = sample_tokens(shape.T, 16, seed=3)
+    same = np.all(np.sort(idx.cpu().numpy()[tokens], 1) == np.sort(ridx[tokens], 1), axis=1)
+    assert same.mean() > 0.8
+    tokens = tokens[same]
+    wc = {k: v.cpu() for k, v in w.items()}
+    ref, _, _ = oracle.layer_forward(x.cpu(), ref_logits, *(wc[k] for k in ("w_gate", "w_up", "w_down", "ws_gate",
+                                                                             "ws_up", "ws_down")),
+                                     K=shape.K, scaling=shape.scaling, tokens=tokens)
+    check_layer(out, ref, rows=tokens, what="gated prefill")
