@@ -348,11 +348,11 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
   cudaError_t e = launch_permute_index(topk_idx, TK, cfg->E, ws, counts, offsets, perm_src,
                                        flat_to_perm, h->status, s);
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, perm_src, cfg->K, TK, x_perm,
-                           h->status, s);
+    e = launch_scatter_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, flat_to_perm, cfg->K, TK, x_perm,
+                            h->status, s);
   if (e == cudaSuccess && mx)
-    e = launch_gather_rows(x_scale, cfg->T, cfg->H / 32, perm_src, cfg->K, TK, x_perm_scale,
-                           h->status, s);
+    e = launch_scatter_rows(x_scale, cfg->T, cfg->H / 32, flat_to_perm, cfg->K, TK, x_perm_scale,
+                            h->status, s);
   return cuda_status(e);
 }
 
@@ -587,7 +587,7 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
                              perm_src, flat_to_perm, h->status, sm);
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, T, mx ? H : H * 2, perm_src, K, TK, x_perm, h->status, sm);
+    e = launch_scatter_rows(x, T, mx ? H : H * 2, flat_to_perm, K, TK, x_perm, h->status, sm);
   if (e == cudaSuccess && mx)
     e = launch_gather_scale_atoms(xq_s, T, H, perm_src, K, offsets, E, TK,
                                   at<uint8_t>(ws, L.x_perm_s), h->status, sm);

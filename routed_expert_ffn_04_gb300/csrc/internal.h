@@ -40,9 +40,10 @@ cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* s
                                  int32_t* flat_to_perm, int* status, cudaStream_t s);
 // dst[r, :] = src[perm_src[r] / K, :] for r < TK; rows are row_bytes long
 // (a multiple of 16). A perm_src entry outside [0, TK) gives a zero row.
-cudaError_t launch_gather_rows(const void* src, int src_rows, int row_bytes,
-                               const int32_t* perm_src, int K, int TK, void* dst, int* status,
-                               cudaStream_t s);
+// x_perm[flat_to_perm[t*K+k]] = x[t] for every token t and slot k: each
+// source row read once (row_bytes a multiple of 4).
+cudaError_t launch_scatter_rows(const void* src, int T, int row_bytes, const int32_t* flat_to_perm,
+                                int K, int TK, void* dst, int* status, cudaStream_t s);
 
 // ---- grouped GEMM (gemm.cu)
 enum GemmMode { kModeAuto = 0, kModeWeightsM = 1, kModeTokensM = 2 };

@@ -16,7 +16,8 @@
 // Up to kSmallMaxTK pairs the three run as the phases of one 1024-thread
 // block (perm_small_kernel), with the per-warp counters in shared memory: the
 // same counting sort, one launch instead of three.
-// A fourth kernel gathers rows with 16-byte vector copies.
+// A fourth kernel copies each token's row to its K permuted places with
+// 16-byte vector copies, reading the row once.
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
@@ -148,6 +149,8 @@ __global__ void __launch_bounds__(kWarps * 32) perm_scatter_kernel(
     if (e >= 0) {
       perm_src[pos] = f;
       flat_to_perm[f] = pos;
+    } else if (f < TK) {
+      flat_to_perm[f] = -1;  // an invalid expert id (reported by the histogram): no row
     }
   }
 }
@@ -243,41 +246,54 @@ __global__ void __launch_bounds__(kSmallThreads) perm_small_kernel(
       if (e >= 0) {
         perm_src[pos] = f;
         flat_to_perm[f] = pos;
+      } else if (f < TK) {
+        flat_to_perm[f] = -1;  // an invalid expert id (reported in phase 1): no row
       }
     }
   }
 }
 
-// One warp per destination row; each lane copies vectors (16 bytes, or 4
-// for short rows such as MX scale rows), four in flight.
-template <typename V>
-__global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ src, int src_rows,
-                                                          int vecs,
-                                                          const int32_t* __restrict__ perm_src,
-                                                          int K, int TK, V* __restrict__ dst,
-                                                          int* status) {
+// Work unit = (source token t, chunk of 32 x CH vectors of its row), one warp
+// each, grid-stride: the chunk is read once and written to the token's K
+// destination rows (flat_to_perm). Rows of x are then read from DRAM once,
+// where a copy per destination row re-read them K times as the write stream
+// pushed them out of L2. A pair with flat_to_perm = -1 (an invalid expert id,
+// already reported) is skipped; any other index outside [0, TK) is reported.
+template <typename V, int CH>
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const V* __restrict__ src, int T, int vecs,
+                                                           const int32_t* __restrict__ flat_to_perm,
+                                                           int K, int TK, V* __restrict__ dst,
+                                                           int* status) {
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int r = gw; r < TK; r += nw) {
-    const int f = __ldg(perm_src + r);
-    const int t = ((unsigned)f < (unsigned)TK) ? f / K : -1;
-    V* d = dst + (size_t)r * vecs;
-    if (t < 0 || t >= src_rows) {
-      if (lane == 0) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
-      for (int v = lane; v < vecs; v += 32) d[v] = V{};
-      continue;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int chunks = (vecs + 32 * CH - 1) / (32 * CH);
+  const long long units = (long long)T * chunks;
+  for (long long u = gw; u < units; u += nw) {
+    const int t = (int)(u / chunks);
+    const int c0 = (int)(u - (long long)t * chunks) * 32 * CH;
+    int my_p = lane < K ? __ldg(flat_to_perm + (size_t)t * K + lane) : -1;
+    if (lane < K && my_p != -1 && (unsigned)my_p >= (unsigned)TK) {
+      if (c0 == 0) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
+      my_p = -1;
     }
     const V* s = src + (size_t)t * vecs;
-    int v = lane;
-    for (; v + 96 < vecs; v += 128) {
-      const V a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64), a3 = __ldg(s + v + 96);
-      d[v] = a0;
-      d[v + 32] = a1;
-      d[v + 64] = a2;
-      d[v + 96] = a3;
+    V a[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int v = c0 + j * 32 + lane;
+      a[j] = v < vecs ? __ldg(s + v) : V{};
     }
-    for (; v < vecs; v += 32) d[v] = __ldg(s + v);
+    for (int k = 0; k < K; ++k) {
+      const int p = __shfl_sync(0xFFFFFFFFu, my_p, k);
+      if (p < 0) continue;  // warp-uniform
+      V* d = dst + (size_t)p * vecs;
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const int v = c0 + j * 32 + lane;
+        if (v < vecs) d[v] = a[j];
+      }
+    }
   }
 }
 
@@ -322,22 +338,26 @@ cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* s
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const void* src, int src_rows, int row_bytes,
-                               const int32_t* perm_src, int K, int TK, void* dst, int* status,
-                               cudaStream_t s) {
-  if (TK == 0) return cudaSuccess;
-  int blocks = (TK + 7) / 8;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (row_bytes % 16 == 0) {
-    gather_rows_kernel<uint4><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), src_rows,
-                                                     row_bytes / 16, perm_src, K, TK,
-                                                     static_cast<uint4*>(dst), status);
+cudaError_t launch_scatter_rows(const void* src, int T, int row_bytes, const int32_t* flat_to_perm,
+                                int K, int TK, void* dst, int* status, cudaStream_t s) {
+  if (T == 0 || TK == 0) return cudaSuccess;
+  constexpr int kCH = 4;  // 2 KB of a bf16 row per unit with 16-byte vectors
+  const bool v16 = row_bytes % 16 == 0;
+  const int vecs = v16 ? row_bytes / 16 : row_bytes / 4;
+  const long long units = (long long)T * ((vecs + 32 * kCH - 1) / (32 * kCH));
+  const long long want = (units + 7) / 8;  // 8 warps a block
+  const int blocks = want < 152 * 16 ? (int)want : 152 * 16;
+  if (v16) {
+    scatter_rows_kernel<uint4, kCH><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), T, vecs,
+                                                           flat_to_perm, K, TK,
+                                                           static_cast<uint4*>(dst), status);
   } else {
-    gather_rows_kernel<uint32_t><<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(src), src_rows,
-                                                        row_bytes / 4, perm_src, K, TK,
-                                                        static_cast<uint32_t*>(dst), status);
+    scatter_rows_kernel<uint32_t, kCH><<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(src), T,
+                                                              vecs, flat_to_perm, K, TK,
+                                                              static_cast<uint32_t*>(dst), status);
   }
   return cudaGetLastError();
 }
+
 
 }  // namespace moe

@@ -81,10 +81,10 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   cudaError_t e = moe::launch_permute_index(topk_idx, TK, cfg->E, scratch, counts, offsets,
                                             perm_src, flat_to_perm, status, s);
   if (e == cudaSuccess)
-    e = moe::launch_gather_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, perm_src, cfg->K, TK, x_perm,
-                                status, s);
+    e = moe::launch_scatter_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, flat_to_perm, cfg->K, TK,
+                                 x_perm, status, s);
   if (e == cudaSuccess && mx)
-    e = moe::launch_gather_rows(x_scale, cfg->T, cfg->H / 32, perm_src, cfg->K, TK, x_perm_scale,
-                                status, s);
+    e = moe::launch_scatter_rows(x_scale, cfg->T, cfg->H / 32, flat_to_perm, cfg->K, TK,
+                                 x_perm_scale, status, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
