@@ -224,7 +224,10 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
  *                      + shared_out[t] )
  * summed in fp32 in that order and rounded once.
  * y_perm (device): [T*K, H] fp32; topk_w: [T, K] fp32; flat_to_perm: [T*K];
- * shared_out (device, nullable): [T, H] fp32; out (device): [T, H] bf16. */
+ * shared_out (device, nullable): [T, H] fp32; out (device): [T, H] bf16.
+ * A flat_to_perm entry of -1 (a pair moe_permute dropped for an expert id out
+ * of range) adds nothing and is not reported again; any other entry outside
+ * [0, T*K) adds nothing and records MOE_DEV_BAD_PERM_INDEX. */
 MOE_API moe_status_t moe_combine(moe_handle_t h, const moe_config_t* cfg, const float* y_perm,
                                  const float* topk_w, const int32_t* flat_to_perm,
                                  const float* shared_out, void* out, moe_stream_t stream);
@@ -270,13 +273,20 @@ MOE_API moe_status_t moe_pack_mx_scales(moe_handle_t h, const uint8_t* scale0,
  * `main` at entry is waited on by `side`, which runs the shared expert and
  * records a second event that `main` waits on before the combine.
  * side == NULL runs the shared expert on `main` before the routed path.
- * x (device): [T, H] bf16 (MXFP8 mode: quantised inside, per call, with the
- * rule of moe_quantize_mxfp8; weights must then be E4M3 codes + scale atoms,
- * for example moe_quantize_mxfp8 on the bf16 weights then moe_pack_mx_scales).
+ * x (device): [T, H] bf16. In the MX modes (weights then E4M3 / E2M1 codes +
+ * scale atoms, for example moe_quantize_mxfp8 on the bf16 weights then
+ * moe_pack_mx_scales):
+ *   x_scale_or_null == NULL: x is bf16 and is quantised inside, per call,
+ *     with the rule of moe_quantize_mxfp8;
+ *   x_scale_or_null != NULL: x already holds E4M3 codes [T, H] (uint8) and
+ *     x_scale_or_null their E8M0 scales [T, H/32], row-major, as
+ *     moe_quantize_mxfp8 writes them; nothing is re-quantised.
+ * bf16 mode: x_scale_or_null must be NULL (MOE_ERR_INVALID_ARG otherwise).
  * logits (device): [T, E] fp32. out (device): [T, H] bf16.
  * ws (device): at least moe_workspace_size bytes. */
 MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
-                                       const moe_weights_t* w, const void* x, const float* logits,
+                                       const moe_weights_t* w, const void* x,
+                                       const uint8_t* x_scale_or_null, const float* logits,
                                        void* out, void* ws, size_t ws_bytes, moe_stream_t main,
                                        moe_stream_t side);
 
@@ -348,9 +358,14 @@ MOE_API moe_status_t moe_read_stage_times(moe_handle_t h, float* ms, int* n_call
  * Limit: E * ceil(T*K / 256) <= MOE_PERMUTE_STATIC_MAX_HIST_INTS (for E = 192
  * and K = 8: T <= 43690); larger sizes return MOE_ERR_WORKSPACE before any
  * launch.
+ * MXFP8 and W4A8 configs move the 1-byte E4M3 rows of x and their E8M0
+ * scales exactly as moe_permute does (same H rule: H % 128 == 0).
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture. The call never allocates or frees device memory.
+ * device current) and caches it for the life of the process; make that first
+ * call before any stream capture. The cache does not survive cudaDeviceReset:
+ * do not call this entry point on a device after resetting it. The caller's
+ * current device is restored before the call returns. The call never
+ * allocates or frees device memory.
  * All calls on a device share the one array and each call overwrites it:
  * calls that overlap on the GPU (different streams, no ordering between
  * them) race and give undefined results. Nothing in the array needs to

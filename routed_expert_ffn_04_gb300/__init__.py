@@ -82,7 +82,7 @@ def load(build_if_missing: bool = False):
         "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
         "moe_quantize_mxfp4": [P, P, ctypes.c_int64, I, P, P, P],
         "moe_pack_mx_scales": [P, P, P, ctypes.c_int64, I, P, P],
-        "moe_layer_forward": [P, P, P, P, P, P, P, S, P, P],
+        "moe_layer_forward": [P, P, P, P, P, P, P, P, S, P, P],
         "moe_layer_forward_host": [P, P, P, P, P, P, P, S, P, P],
         "moe_get_device_status": [P, ctypes.POINTER(I), P],
         "moe_read_stage_times": [P, ctypes.POINTER(F), ctypes.POINTER(I)],
@@ -313,10 +313,12 @@ def make_weights(w: dict) -> Weights:
     return ws
 
 
-def layer_forward(h: Handle, cfg: Config, weights: Weights, x, logits, out, ws, main=None, side=None):
+def layer_forward(h: Handle, cfg: Config, weights: Weights, x, logits, out, ws, main=None, side=None,
+                  x_scale=None):
+    """x_scale: E8M0 scales [T, H/32] when x already holds MXFP8 E4M3 codes (MX configs only)."""
     side_p = ctypes.c_void_p(side.cuda_stream) if side is not None else None
-    _check(load().moe_layer_forward(h.ptr, ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(logits), _p(out),
-                                    _p(ws), ws.numel() * ws.element_size(), _stream(main), side_p),
+    _check(load().moe_layer_forward(h.ptr, ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(x_scale), _p(logits),
+                                    _p(out), _p(ws), ws.numel() * ws.element_size(), _stream(main), side_p),
            "moe_layer_forward")
 
 
@@ -348,8 +350,10 @@ class MoELayer:
         self.weights = make_weights(weights)
         self.side = torch.cuda.Stream(device=self.device) if side_stream else None
 
-    def __call__(self, x, logits, out=None, main=None):
+    def __call__(self, x, logits, out=None, main=None, x_scale=None):
+        """x: [T, H] bf16, or (MX layers, with x_scale) MXFP8 E4M3 codes with their E8M0 scales."""
         if out is None:
             out = torch.empty((self.shape.T, self.shape.H), dtype=torch.bfloat16, device=self.device)
-        layer_forward(self.handle, self.cfg, self.weights, x, logits, out, self.ws, main=main, side=self.side)
+        layer_forward(self.handle, self.cfg, self.weights, x, logits, out, self.ws, main=main, side=self.side,
+                      x_scale=x_scale)
         return out

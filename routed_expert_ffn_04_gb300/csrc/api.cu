@@ -469,12 +469,13 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
   moe_status_t st = check_handle(h);
   if (st != MOE_OK) return st;
   return cuda_status(
-      launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr, nullptr,
+      launch_mx_quantize(in_bf16, rows, cols, q, scale, nullptr,
                          static_cast<cudaStream_t>(stream)));
 }
 
 static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
-                                       const moe_weights_t* w, const void* x, const float* logits,
+                                       const moe_weights_t* w, const void* x,
+                                       const uint8_t* x_scale, const float* logits,
                                        const void* w_router, void* out, void* ws, size_t ws_bytes,
                                        moe_stream_t main, moe_stream_t side) {
   moe_status_t st = check_cfg(cfg);
@@ -487,6 +488,10 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
   const bool mx = is_mx(cfg->dtype);
   const bool w4 = cfg->dtype == MOE_MXFP4_W4A8;  // routed experts E2M1; shared stays E4M3
+  // Pre-quantised activations: only in MX mode, and only with given logits
+  // (the router reads bf16 x).
+  if (x_scale && (!mx || w_router)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_scale)) return MOE_ERR_INVALID_ARG;
   if (mx && (!w->s_gate || !w->s_down)) return MOE_ERR_INVALID_ARG;
   if (w4 && !weights_aligned32(w->w_gate, w->w_up, w->w_down)) return MOE_ERR_INVALID_ARG;
   if (mx && has_shared && (!w->ss_gate || !w->ss_down)) return MOE_ERR_INVALID_ARG;
@@ -533,12 +538,20 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   cudaError_t e = cudaSuccess;
   mark(0, sm);
   const void* x_gate = x;  // the router reads x as given (bf16)
-  uint8_t* xq_s = nullptr;  // MXFP8: scales of the quantised x
-  if (mx) {  // dynamic MXFP8 quantisation of x (E4M3 codes + E8M0 scales)
+  const uint8_t* xq_s = nullptr;  // MX: row-major E8M0 scales of the E4M3 x
+  if (mx && x_scale) {
+    // The caller's E4M3 codes and scales; the shared expert still needs its
+    // scales as atoms (one group of T rows).
+    xq_s = x_scale;
+    if (has_shared)
+      e = launch_gather_scale_atoms(x_scale, T, H, nullptr, 1, nullptr, 1, T,
+                                    at<uint8_t>(ws, L.x_mx_atoms), h->status, sm);
+  } else if (mx) {  // dynamic MXFP8 quantisation of x (E4M3 codes + E8M0 scales)
     void* xq = at<void>(ws, L.x_mx);
-    xq_s = at<uint8_t>(ws, L.x_mx_s);
-    e = launch_mx_quantize(x, T, H, static_cast<uint8_t*>(xq), xq_s,
-                           has_shared ? at<uint8_t>(ws, L.x_mx_atoms) : nullptr, nullptr, sm);
+    uint8_t* s = at<uint8_t>(ws, L.x_mx_s);
+    e = launch_mx_quantize(x, T, H, static_cast<uint8_t*>(xq), s,
+                           has_shared ? at<uint8_t>(ws, L.x_mx_atoms) : nullptr, sm);
+    xq_s = s;
     x = xq;
   }
   cudaStream_t s_sh = ss ? ss : sm;
@@ -626,11 +639,13 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
 }
 
 MOE_API moe_status_t moe_layer_forward(moe_handle_t h, const moe_config_t* cfg,
-                                       const moe_weights_t* w, const void* x, const float* logits,
+                                       const moe_weights_t* w, const void* x,
+                                       const uint8_t* x_scale_or_null, const float* logits,
                                        void* out, void* ws, size_t ws_bytes, moe_stream_t main,
                                        moe_stream_t side) {
   if (cfg && cfg->T > 0 && !logits) return MOE_ERR_INVALID_ARG;
-  return layer_forward_impl(h, cfg, w, x, logits, nullptr, out, ws, ws_bytes, main, side);
+  return layer_forward_impl(h, cfg, w, x, x_scale_or_null, logits, nullptr, out, ws, ws_bytes,
+                            main, side);
 }
 
 MOE_API moe_status_t moe_layer_forward_gated(moe_handle_t h, const moe_config_t* cfg,
@@ -638,7 +653,8 @@ MOE_API moe_status_t moe_layer_forward_gated(moe_handle_t h, const moe_config_t*
                                              const void* x, void* out, void* ws, size_t ws_bytes,
                                              moe_stream_t main, moe_stream_t side) {
   if (!w_router || (cfg && cfg->E > 256 && cfg->E % 32)) return MOE_ERR_INVALID_ARG;
-  return layer_forward_impl(h, cfg, w, x, nullptr, w_router, out, ws, ws_bytes, main, side);
+  return layer_forward_impl(h, cfg, w, x, nullptr, nullptr, w_router, out, ws, ws_bytes, main,
+                            side);
 }
 
 MOE_API moe_status_t moe_gate_route(moe_handle_t h, const moe_config_t* cfg, const void* x,
@@ -676,7 +692,7 @@ MOE_API moe_status_t moe_layer_forward_host(moe_handle_t h, const moe_config_t* 
   cudaError_t e = cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, sm);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ld, logits_host, lb, cudaMemcpyHostToDevice, sm);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  st = moe_layer_forward(h, cfg, w, xd, ld, od, ws, ws_bytes, main, side);
+  st = moe_layer_forward(h, cfg, w, xd, nullptr, ld, od, ws, ws_bytes, main, side);
   if (st != MOE_OK) return st;
   e = cudaMemcpyAsync(out_host, od, xb, cudaMemcpyDeviceToHost, sm);
   if (e == cudaSuccess) e = cudaStreamSynchronize(sm);

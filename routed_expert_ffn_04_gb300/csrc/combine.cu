@@ -48,7 +48,9 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
       int32_t p = flat_to_perm[(size_t)t * K + threadIdx.x];
       float w = topk_w[(size_t)t * K + threadIdx.x];
       if ((unsigned)p >= (unsigned)TK) {
-        atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
+        // -1 marks a pair the permutation dropped (an expert id out of
+        // range, already reported there): it adds nothing, silently.
+        if (p != -1) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
         p = -1;
       }
       sp[threadIdx.x] = p;
@@ -107,7 +109,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       int32_t p = flat_to_perm[(size_t)t * K + threadIdx.x];
       float w = topk_w[(size_t)t * K + threadIdx.x];
       if ((unsigned)p >= (unsigned)TK) {
-        atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
+        // -1 marks a pair the permutation dropped (an expert id out of
+        // range, already reported there): it adds nothing, silently.
+        if (p != -1) atomicCAS(status, 0, MOE_DEV_BAD_PERM_INDEX);
         p = -1;
       }
       sp[threadIdx.x] = p;

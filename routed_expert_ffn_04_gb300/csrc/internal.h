@@ -19,6 +19,10 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Both MX dtypes carry E4M3 activations (1 byte per element) with one E8M0
+// scale per 32 elements; they differ only in the routed experts' weights.
+inline bool is_mx_dtype(int dtype) { return dtype == MOE_MXFP8_E4M3 || dtype == MOE_MXFP4_W4A8; }
+
 // ---- routing (route.cu)
 cudaError_t launch_route(const float* logits, int T, int E, int K, float scaling, int route_norm,
                          int32_t* topk_idx, float* topk_w, cudaStream_t s);
@@ -115,12 +119,11 @@ cudaError_t launch_combine(const float* y_perm, const float* topk_w, const int32
                            cudaStream_t s);
 
 // ---- MX quantiser (mxquant.cu)
-// q / scale / atoms / deq may each be null. scale: row-major [rows, cols/32];
+// q / scale / atoms may each be null. scale: row-major [rows, cols/32];
 // atoms: the scale atoms of the rows as one group (cols % 128 == 0; the rows
-// of the last 128-row block past `rows` are left untouched); deq: the
-// dequantised values as bf16.
+// of the last 128-row block past `rows` are left untouched).
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, uint8_t* atoms, void* deq, cudaStream_t s);
+                               uint8_t* scale, uint8_t* atoms, cudaStream_t s);
 
 // MXFP4: q [rows, cols/2] packed E2M1 codes (element 2j in the low nibble),
 // scale [rows, cols/32] row-major.
@@ -141,10 +144,6 @@ cudaError_t launch_gather_scale_atoms(const uint8_t* src, int src_rows, int cols
                                       int G, int rows, uint8_t* out, int* status, cudaStream_t s);
 // Bytes of activation atoms for `rows` rows in at most `groups` groups.
 size_t scale_atom_bytes(int64_t rows, int groups, int cols);
-// out[r, c] = bf16(e4m3(q[r, c]) * 2^(scale[r, c/32] - 127)).
-cudaError_t launch_mx_dequantize(const uint8_t* q, const uint8_t* scale, int64_t rows, int cols,
-                                 void* out_bf16, cudaStream_t s);
-
 // ---- self-test of the bounded wait (gemm.cu)
 cudaError_t launch_selftest_wait(int* status, uint64_t limit_ns, cudaStream_t s);
 

@@ -11,8 +11,7 @@
 //
 // One thread per block of 32: 64 bytes in (four 16-byte loads), 32 code
 // bytes out (two 16-byte stores) and one scale byte, row-major and/or in the
-// scale atoms of the block-scaled GEMM (mx_layout.cuh); optionally the
-// dequantised block as bf16 (exact: an E4M3 value times a power of two).
+// scale atoms of the block-scaled GEMM (mx_layout.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -28,8 +27,7 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
                                                        long long nblocks,
                                                        uint4* __restrict__ q,
                                                        uint8_t* __restrict__ scale,
-                                                       uint8_t* __restrict__ atoms, int nb,
-                                                       uint4* __restrict__ deq) {
+                                                       uint8_t* __restrict__ atoms, int nb) {
   const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nblocks) return;
   uint4 raw[4];
@@ -70,13 +68,6 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const uint4* __restrict__
     q[b * 2] = make_uint4(words[0], words[1], words[2], words[3]);
     q[b * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
   }
-  if (deq) {
-    uint32_t o[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) e4m3x4_to_bf16(words[j], code, o[2 * j], o[2 * j + 1]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) deq[b * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-  }
 }
 
 // MXFP4: one thread per block of 32 bf16 -> 16 bytes of packed E2M1 codes
@@ -110,33 +101,17 @@ __global__ void __launch_bounds__(256) mx4_quant_kernel(const uint4* __restrict_
   q[b] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
-__global__ void __launch_bounds__(256) mx_dequant_kernel(const uint4* __restrict__ q,
-                                                         const uint8_t* __restrict__ scale,
-                                                         long long nblocks,
-                                                         uint4* __restrict__ out) {
-  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= nblocks) return;
-  const uint4 q0 = __ldg(q + b * 2), q1 = __ldg(q + b * 2 + 1);
-  const int sc = scale[b];
-  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-  uint32_t o[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) e4m3x4_to_bf16(words[j], sc, o[2 * j], o[2 * j + 1]);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) out[b * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-}
-
 }  // namespace
 
 cudaError_t launch_mx_quantize(const void* in_bf16, int64_t rows, int cols, uint8_t* q,
-                               uint8_t* scale, uint8_t* atoms, void* deq, cudaStream_t s) {
+                               uint8_t* scale, uint8_t* atoms, cudaStream_t s) {
   const long long nblocks = (long long)rows * (cols / 32);
   if (nblocks == 0) return cudaSuccess;
   if (atoms && cols % 128) return cudaErrorInvalidValue;
   const long long grid = (nblocks + 255) / 256;
   mx_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
                                                  reinterpret_cast<uint4*>(q), scale, atoms,
-                                                 cols / 32, static_cast<uint4*>(deq));
+                                                 cols / 32);
   return cudaGetLastError();
 }
 
@@ -147,16 +122,6 @@ cudaError_t launch_mx4_quantize(const void* in_bf16, int64_t rows, int cols, uin
   const long long grid = (nblocks + 255) / 256;
   mx4_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint4*>(in_bf16), nblocks,
                                                   reinterpret_cast<uint4*>(q), scale);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mx_dequantize(const uint8_t* q, const uint8_t* scale, int64_t rows, int cols,
-                                 void* out_bf16, cudaStream_t s) {
-  const long long nblocks = (long long)rows * (cols / 32);
-  if (nblocks == 0) return cudaSuccess;
-  const long long grid = (nblocks + 255) / 256;
-  mx_dequant_kernel<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(q), scale, nblocks,
-                                                   static_cast<uint4*>(out_bf16));
   return cudaGetLastError();
 }
 

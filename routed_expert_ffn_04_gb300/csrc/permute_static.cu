@@ -32,7 +32,10 @@ ScratchAddr g_addr[kMaxDevices];
 
 // Device address of g_permute_scratch on `device` (which must be current).
 // In host code the array's name is only a host-side stand-in, so the address
-// is looked up once per device and cached.
+// is looked up once per device and cached for the life of the process. The
+// cache does not survive cudaDeviceReset (the array is re-created at a new
+// address): a process that resets a device must not call this entry point
+// on it again.
 cudaError_t scratch_address(int device, void** out) {
   ScratchAddr& a = g_addr[device];
   std::call_once(a.once, [&a] { a.err = cudaGetSymbolAddress(&a.ptr, g_permute_scratch); });
@@ -51,7 +54,8 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   size_t need = 0;
   moe_status_t st = moe_permute_workspace_size(cfg, &need);  // validates cfg
   if (st != MOE_OK) return st;
-  const bool mx = cfg->dtype == MOE_MXFP8_E4M3;
+  // MXFP8 and W4A8 both move 1-byte E4M3 rows plus their E8M0 scales.
+  const bool mx = moe::is_mx_dtype(cfg->dtype);
   const bool any = cfg->T > 0;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (any && (!x || !topk_idx || !perm_src || !flat_to_perm || !x_perm)) return MOE_ERR_INVALID_ARG;
@@ -60,7 +64,6 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (mx && (!aligned16(x_scale) || !aligned16(x_perm_scale))) return MOE_ERR_INVALID_ARG;
-  if (mx && cfg->H % 512) return MOE_ERR_UNSUPPORTED;
   // The histogram has E * ceil(T*K / 256) entries; the fixed array caps it.
   const long long nw = ((long long)cfg->T * cfg->K + 255) / 256;
   if ((long long)cfg->E * (nw > 0 ? nw : 1) > MOE_PERMUTE_STATIC_MAX_HIST_INTS)
@@ -72,8 +75,13 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
   if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
+  // The caller's current device is put back on every return below.
+  auto done = [cur, dev](moe_status_t r) {
+    if (cur != dev && cudaSetDevice(cur) != cudaSuccess && r == MOE_OK) r = MOE_ERR_CUDA;
+    return r;
+  };
   void* scratch = nullptr;
-  if (scratch_address(dev, &scratch) != cudaSuccess || scratch == nullptr) return MOE_ERR_CUDA;
+  if (scratch_address(dev, &scratch) != cudaSuccess || scratch == nullptr) return done(MOE_ERR_CUDA);
 
   int* status = moe::handle_status_word(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -86,5 +94,5 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   if (e == cudaSuccess && mx)
     e = moe::launch_scatter_rows(x_scale, cfg->T, cfg->H / 32, flat_to_perm, cfg->K, TK,
                                  x_perm_scale, status, s);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return done(e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA);
 }

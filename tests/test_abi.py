@@ -109,9 +109,13 @@ def test_small_workspace_rejected(lib):
         setattr(w, k, 1 << 20)
     need = moe.workspace_size(cfg)
     P = ctypes.c_void_p
-    rc = lib.moe_layer_forward(None, ctypes.byref(cfg), ctypes.byref(w), P(1 << 20), P(1 << 20), P(1 << 20),
+    rc = lib.moe_layer_forward(None, ctypes.byref(cfg), ctypes.byref(w), P(1 << 20), None, P(1 << 20), P(1 << 20),
                                P(1 << 20), need - 256, None, None)
     assert rc == moe.MOE_ERR_WORKSPACE
+    # Pre-quantised activations (x_scale_or_null) only exist in the MX modes.
+    rc = lib.moe_layer_forward(None, ctypes.byref(cfg), ctypes.byref(w), P(1 << 20), P(1 << 20), P(1 << 20),
+                               P(1 << 20), P(1 << 20), need, None, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
     rc = lib.moe_grouped_swiglu_gemm(None, 4, 100, 256, 128, 0, P(256), None, P(256), P(256), P(256), P(256),
                                      None, None, None, P(256), P(256), 10, None)
     assert rc == moe.MOE_ERR_WORKSPACE

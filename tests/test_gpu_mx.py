@@ -15,7 +15,7 @@ import torch
 import oracle
 import routed_expert_ffn_04_gb300 as moe
 import synth
-from gpu_common import cfg_of, sample_tokens
+from gpu_common import cfg_of, edge_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -185,12 +185,39 @@ def test_mx_layer_ragged_shape(handle, mode):
     _check(out.float().cpu().numpy(), ref, f"ragged mx mode={mode}")
 
 
-def test_mx_layer_full_size_sampled(handle):
+def test_mx_layer_full_size_tile_edges(handle):
     shape = synth.WORKLOADS["mxfp8"]
     x, logits = synth.make_activations(shape, device="cuda", seed=0)
     w = synth.make_weights(shape, device="cuda", seed=0)
     out = _run_mx_layer(handle, shape, x, logits, w)
-    tokens = sample_tokens(shape.T, 16, seed=2)
+    ridx, _ = oracle.route(logits.cpu().numpy(), shape.K, shape.scaling)
+    tokens = edge_tokens(ridx, shape.E, sample=16, seed=2)
     ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _mx_weights_oracle(w), K=shape.K, scaling=shape.scaling,
                                   tokens=tokens)
     _check(out.float().cpu().numpy()[tokens], ref, "mxfp8 workload")
+
+
+@pytest.mark.parametrize("dtype", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("side", [True, False])
+def test_prequantised_input_matches_bf16_input(handle, dtype, side):
+    # moe_layer_forward with x already MXFP8 (codes + scales from
+    # moe_quantize_mxfp8) gives the same bits as the layer that quantises the
+    # bf16 x itself: the same codes and scales reach the same kernels.
+    shape = synth.MoEShape("pre", T=300, H=512, E=24, K=4, I=256, I_shared=128, dtype=dtype)
+    x, logits = synth.make_activations(shape, device="cuda", seed=9)
+    w = synth.make_weights(shape, device="cuda", seed=9)
+    layer = moe.MoELayer(shape, w, device=0, side_stream=side)
+    a = layer(x, logits).clone()
+    xq, xs = moe.quantize_mx(layer.handle, x)
+    b = layer(xq, logits, x_scale=xs).clone()
+    torch.cuda.synchronize()
+    assert layer.handle.device_status() == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # And both match the MX oracle.
+    if dtype == "mxfp4":  # routed weights MXFP4, shared W8A8
+        wo = {k: (oracle.mxfp4_quantize(v.cpu()) if k.startswith("w_") else oracle.mx_quantize(v.cpu()))
+              for k, v in w.items()}
+    else:
+        wo = _mx_weights_oracle(w)
+    ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), wo, K=shape.K, scaling=shape.scaling, w4=dtype == "mxfp4")
+    _check(b.float().cpu().numpy(), ref, f"pre-quantised {dtype}")

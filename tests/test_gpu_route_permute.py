@@ -144,3 +144,32 @@ def test_bad_expert_id_is_reported(handle):
     _permute(handle, shape, idx, x)
     assert handle.device_status() == 16  # MOE_DEV_BAD_EXPERT_ID
     assert handle.device_status() == 0   # cleared by the read
+
+
+def test_combine_skips_dropped_pairs_silently(handle):
+    # A pair with an expert id out of range is dropped by the permutation
+    # (reported once there, flat_to_perm = -1). The combine then adds the
+    # token's other slots only and reports nothing more.
+    shape = synth.MoEShape("bad", T=4, H=64, E=8, K=2, I=64, I_shared=0)
+    idx = torch.tensor([[0, 1], [2, 99], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    handle.device_status()
+    _, _, _, f2p, _ = _permute(handle, shape, idx, x)
+    assert handle.device_status() == 16  # MOE_DEV_BAD_EXPERT_ID, from the permutation
+    assert f2p[3] == -1
+    g = torch.Generator(device="cpu").manual_seed(5)
+    y = torch.randn((shape.T * shape.K, shape.H), generator=g, dtype=torch.float32)
+    w = torch.rand((shape.T, shape.K), generator=g, dtype=torch.float32)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+    moe.combine(handle, cfg_of(shape), y.cuda(), w.cuda(), torch.from_numpy(f2p).cuda(), None, out)
+    torch.cuda.synchronize()
+    assert handle.device_status() == 0
+    ref = np.zeros((shape.T, shape.H))
+    for t in range(shape.T):
+        for k in range(shape.K):
+            p = f2p[t * shape.K + k]
+            if p >= 0:
+                ref[t] += float(w[t, k]) * y[p].double().numpy()
+    got = out.float().cpu().numpy()
+    # One bf16 rounding of an fp32 sum: within a bf16 half-ulp plus fp32 error.
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5)
