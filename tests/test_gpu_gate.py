@@ -20,7 +20,7 @@ import torch
 import oracle
 import routed_expert_ffn_04_gb300 as moe
 import synth
-from gpu_common import check_layer, cfg_of, sample_tokens
+from gpu_common import check_layer, cfg_of, edge_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -158,7 +158,7 @@ def test_gated_mx_layer_matches_oracle(handle, dtype):
     assert np.all(np.isfinite(got)) and rel <= 3e-2 and np.abs(got - r).max() <= 2e-2, (rel, np.abs(got - r).max())
 
 
-def test_gated_full_prefill_sampled(handle):
+def test_gated_full_prefill_tile_edges(handle):
     # The bench's gated prefill line: T = 8192 takes the tcgen05 gating path.
     shape = synth.WORKLOADS["prefill"]
     x, _ = synth.make_activations(shape, device="cuda", seed=0)
@@ -174,7 +174,7 @@ def test_gated_full_prefill_sampled(handle):
     assert layer.handle.device_status() == 0
     ref_logits = oracle.gate(x.cpu(), wr.cpu()).astype(np.float32)
     ridx, _ = oracle.route(ref_logits, shape.K, shape.scaling)
-    tokens = sample_tokens(shape.T, 16, seed=3)
+    tokens = edge_tokens(ridx, shape.E, sample=16, seed=3)
     same = np.all(np.sort(idx.cpu().numpy()[tokens], 1) == np.sort(ridx[tokens], 1), axis=1)
     assert same.mean() > 0.8
     tokens = tokens[same]

@@ -16,7 +16,7 @@ import torch
 import oracle
 import routed_expert_ffn_04_gb300 as moe
 import synth
-from gpu_common import sample_tokens
+from gpu_common import edge_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -122,12 +122,13 @@ def test_w4a8_layer_ragged_shape(handle):
     _check(out.float().cpu().numpy(), ref, "ragged w4a8")
 
 
-def test_w4a8_layer_full_size_sampled(handle):
+def test_w4a8_layer_full_size_tile_edges(handle):
     shape = synth.WORKLOADS["mxfp4"]
     x, logits = synth.make_activations(shape, device="cuda", seed=0)
     w = synth.make_weights(shape, device="cuda", seed=0)
     out = _run_layer(shape, x, logits, w)
-    tokens = sample_tokens(shape.T, 16, seed=4)
+    ridx, _ = oracle.route(logits.cpu().numpy(), shape.K, shape.scaling)
+    tokens = edge_tokens(ridx, shape.E, sample=16, seed=4)
     ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _w4a8_weights_oracle(w), K=shape.K, scaling=shape.scaling,
                                   tokens=tokens, w4=True)
     _check(out.float().cpu().numpy()[tokens], ref, "mxfp4 workload")

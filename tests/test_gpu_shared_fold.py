@@ -9,9 +9,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import routed_expert_ffn_04_gb300 as moe
 import synth
-from gpu_common import check_layer, make_problem, oracle_layer, run_layer, sample_tokens
+from gpu_common import check_layer, edge_tokens, make_problem, oracle_layer, run_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -41,11 +42,12 @@ def test_decode_folded_all_tokens(handle):
     check_layer(out, ref, what="decode folded")
 
 
-def test_prefill_folded_sampled(handle):
+def test_prefill_folded_tile_edges(handle):
     shape = synth.WORKLOADS["prefill"]
     x, logits, w = make_problem(shape, seed=0, device="cuda")
     out = run_layer(handle, shape, x, logits, w, fold=True)
-    tokens = sample_tokens(shape.T, 16, seed=3)
+    ridx, _ = oracle.route(logits.cpu().numpy(), shape.K, shape.scaling)
+    tokens = edge_tokens(ridx, shape.E, sample=16, seed=3)
     ref, _, _ = oracle_layer(shape, x.cpu(), logits, {k: v.cpu() for k, v in w.items()}, tokens=tokens)
     check_layer(out, ref, rows=tokens, what="prefill folded")
 
