@@ -63,6 +63,12 @@ def parse():
     ap.add_argument("--shared-fold", action="store_true",
                     help="run the shared expert as one more group of the routed GEMMs (bf16, I_shared == I)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--gemm-mode", type=int, default=0,
+                    help="MOE_OPT_GEMM_MODE for the timed calls (0 automatic, 1 weights-as-M, 2 tokens-as-M, 3 CTA pair)")
+    ap.add_argument("--ab-gemm-modes", default="",
+                    help="comma-separated GEMM modes to time against each other (interleaved graph replays)")
+    ap.add_argument("--shared-sms-sweep", default="",
+                    help="comma-separated MOE_OPT_SHARED_SMS values to add to the overlap measurement")
     ap.add_argument("--experts", type=int, default=None,
                     help="override the routed expert count (smaller device footprint for profiler captures)")
     return ap.parse_args()
@@ -280,6 +286,123 @@ def time_graph(call, args, main, dev, world):
     return g0.elapsed_time(g1) / args.steps
 
 
+def _spread(ms):
+    a = np.asarray(ms)
+    return {"median": round(float(np.median(a)), 5), "p10": round(float(np.percentile(a, 10)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5)}
+
+
+def interleaved_replays(variants, main, dev, rounds=200):
+    """Capture one CUDA graph per variant (name -> (setup, call); setup runs
+    before the capture, e.g. to set a handle option baked into the launches)
+    and time their replays interleaved round by round, the first of each
+    round rotating; returns name -> list of ms."""
+    import torch
+
+    graphs = {}
+    for name, (setup, fn) in variants.items():
+        setup()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(main)
+        with torch.cuda.stream(cap):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        torch.cuda.synchronize()
+        graphs[name] = g
+    names = list(graphs)
+    times = {n: [] for n in names}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for r in range(rounds + 5):
+        order = names[r % len(names):] + names[:r % len(names)]
+        for n in order:
+            e0.record(main)
+            graphs[n].replay()
+            e1.record(main)
+            torch.cuda.synchronize()
+            if r >= 5:
+                times[n].append(e0.elapsed_time(e1))
+    return times
+
+
+def measure_gemm_modes(moe, layer, modes, call, main, dev, rounds=200):
+    """The layer with each grouped-GEMM tiling: interleaved graph replays, and
+    per-stage device times from 30 eager calls each."""
+    import torch
+
+    def setter(m):
+        return lambda: layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, m)
+
+    times = interleaved_replays({f"mode{m}": (setter(m), call) for m in modes}, main, dev, rounds)
+    stages = {}
+    for m in modes:
+        layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, m)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
+        for _ in range(30):
+            call()
+        torch.cuda.synchronize()
+        st, _ = layer.handle.stage_times()
+        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
+        stages[f"mode{m}"] = {k: round(v, 5) for k, v in st.items()}
+    layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, 0)
+    return {"method": f"graph replays, {rounds} interleaved rounds; stages from 30 eager calls",
+            "ms": {n: _spread(v) for n, v in times.items()}, "stage_ms": stages}
+
+
+def measure_overlap(moe, layer, shape, cfg, x, logits, w_router, out, main, dev, args, rounds=200):
+    """Shared-expert overlap from interleaved graph replays (see run_ours), and
+    an eager A/B of the side stream at normal and at high priority."""
+    import torch
+
+    cfg_none = moe.make_config(shape.T, shape.H, shape.E, shape.K, shape.I, 0, shape.scaling, shape.route_norm,
+                               cfg.dtype)
+    side_hi = torch.cuda.Stream(device=dev, priority=-1)  # torch's high priority
+
+    def fwd(c, side):
+        if args.gated:
+            moe.layer_forward_gated(layer.handle, c, layer.weights, w_router, x, out, layer.ws, side=side)
+        else:
+            moe.layer_forward(layer.handle, c, layer.weights, x, logits, out, layer.ws, side=side)
+
+    calls = {"two_stream": lambda: fwd(cfg, layer.side), "serial": lambda: fwd(cfg, None),
+             "no_shared": lambda: fwd(cfg_none, None)}
+    sms = {}
+    for v in filter(None, args.shared_sms_sweep.split(",")):
+        calls[f"two_stream_sms{int(v)}"] = calls["two_stream"]
+        sms[f"two_stream_sms{int(v)}"] = int(v)
+    def sms_setter(k):  # the SM split between the streams is baked into the captured grids
+        return lambda: layer.handle.set_option(moe.MOE_OPT_SHARED_SMS, k)
+
+    times = interleaved_replays({n: (sms_setter(sms.get(n, 0)), fn) for n, fn in calls.items()}, main, dev, rounds)
+    layer.handle.set_option(moe.MOE_OPT_SHARED_SMS, 0)
+    names = list(times)
+    med = {n: float(np.median(times[n])) for n in names}
+    alone = med["serial"] - med["no_shared"]
+    res = {"method": f"graph replays, {rounds} interleaved rounds, stage timing off",
+           "ms": {n: _spread(times[n]) for n in names},
+           "shared_alone_ms": round(alone, 5),
+           "hidden_fraction": round((med["serial"] - med["two_stream"]) / alone, 3) if alone > 0 else None}
+    # Eager calls: the side stream at normal and at high priority, interleaved.
+    ev = {k: [] for k in ("normal", "high")}
+    pairs = {"normal": layer.side, "high": side_hi}
+    for r in range(rounds + 5):
+        for k in (("normal", "high") if r % 2 == 0 else ("high", "normal")):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            fwd(cfg, pairs[k])
+            e1.record(main)
+            torch.cuda.synchronize()
+            if r >= 5:
+                ev[k].append(e0.elapsed_time(e1))
+    res["eager_side_priority_ms"] = {k: _spread(v) for k, v in ev.items()}
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -298,6 +421,7 @@ def run_ours(args):
     x, logits = synth.make_activations(shape, device=dev, seed=rank)
     w = synth.make_weights(shape, device=dev, seed=0)
     layer = moe.MoELayer(shape, w, device=local)
+    layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, args.gemm_mode)
     if args.shared_fold:
         layer.handle.set_option(moe.MOE_OPT_SHARED_FOLD, 1)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
@@ -381,34 +505,19 @@ def run_ours(args):
     e2e_ms = dist_max(e2e_ms, world, dev)
 
     # How much of the shared expert the second stream hides (the two-stream
-    # timeline check): the same eager calls with the shared expert serial on
-    # the main stream, where its stage is the shared MLP alone.
+    # timeline check, measured rather than assumed): graph replays of three
+    # captured calls, interleaved round by round with stage timing off --
+    # the two-stream layer, the same layer with the shared expert serial on
+    # the main stream, and the layer without a shared expert. The shared MLP
+    # alone costs serial - none; the second stream hides (serial - two) of it.
     overlap = None
     if shape.I_shared and not (args.shared_fold and shape.dtype == "bf16"):
-        def call_serial():
-            if args.gated:
-                moe.layer_forward_gated(layer.handle, cfg, layer.weights, w_router, x, out, layer.ws, side=None)
-            else:
-                moe.layer_forward(layer.handle, cfg, layer.weights, x, logits, out, layer.ws, side=None)
+        overlap = measure_overlap(moe, layer, shape, cfg, x, logits, w_router, out, main, dev, args)
 
-        n_ov = max(3, min(args.steps, 200))
-        for _ in range(3):
-            call_serial()
-        torch.cuda.synchronize()
-        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(main)
-        for _ in range(n_ov):
-            call_serial()
-        s1.record(main)
-        torch.cuda.synchronize()
-        serial_ms = s0.elapsed_time(s1) / n_ov
-        st_serial, _ = layer.handle.stage_times()
-        layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
-        shared_alone = st_serial["shared"]
-        overlap = {"two_stream_ms": round(eager_ms, 5), "serial_ms": round(serial_ms, 5),
-                   "shared_alone_ms": round(shared_alone, 5),
-                   "hidden_fraction": round((serial_ms - eager_ms) / shared_alone, 3) if shared_alone > 0 else None}
+    gemm_ab = None
+    if args.ab_gemm_modes:
+        gemm_ab = measure_gemm_modes(moe, layer, [int(v) for v in args.ab_gemm_modes.split(",")], call, main, dev)
+        layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, args.gemm_mode)
 
     peaks, peak_src = load_peaks()
     g1_ms = stage_ms["gemm_gate_up"]
@@ -490,11 +599,32 @@ def run_ours(args):
         "clocks": clocks,
         "shared_overlap": overlap,
     }
+    if gemm_ab is not None:
+        result["gemm_mode_ab"] = gemm_ab
     if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
         rate, n, dt, thr = cpu_oracle_rate(shape, x, logits, w, budget_s=12.0)
         result["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                   "sample": f"{n} tokens of the {args.workload} workload (its {shape.T} tokens "
                                             f"cycled) through the fp64 oracle ({dt:.1f} s)"}
+        # The same oracle on one thread: this workload (bounded sample) and
+        # the whole tiny layer.
+        oracle.set_num_threads(1)
+        try:
+            single = {}
+            r1, n1, dt1, _ = cpu_oracle_rate(shape, x, logits, w, budget_s=6.0)
+            single[args.workload] = {"value": round(r1, 3), "unit": "tokens/s",
+                                     "sample": f"{n1} tokens ({dt1:.1f} s)"}
+            tiny = synth.WORKLOADS["tiny"]
+            xt, lt = synth.make_activations(tiny, seed=0)
+            wt = synth.make_weights(tiny, seed=0)
+            rt, nt, dtt, _ = cpu_oracle_rate(tiny, xt, lt, wt, budget_s=0.5, max_tokens=tiny.T)
+            single["tiny"] = {"value": round(rt, 3), "unit": "tokens/s",
+                              "sample": f"the whole tiny layer ({nt} tokens, {dtt * 1e3:.2f} ms)"}
+            result["cpu_baseline"]["single_thread"] = single
+        finally:
+            oracle.set_num_threads(thr)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

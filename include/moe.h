@@ -111,9 +111,13 @@ typedef void* moe_stream_t; /* a cudaStream_t */
 
 /* Options for moe_set_option. */
 typedef enum {
-  /* Grouped GEMM tiling: 0 = automatic (default), 1 = weight rows fill the
-   * 128-row MMA tile and tokens form N (small token counts per expert),
-   * 2 = tokens fill the 128-row MMA tile (large token counts per expert). */
+  /* Grouped GEMM tiling: 0 = automatic (default: 1 up to 48 rows per group
+   * on average, 2 above), 1 = weight rows fill the 128-row MMA tile and
+   * tokens form N (small token counts per expert), 2 = tokens fill the
+   * 128-row MMA tile, 3 = weight rows fill a 256-row MMA spread over a pair
+   * of SMs and up to 128 (GEMM-1) or 256 (GEMM-2) tokens form N (large token
+   * counts per expert; bf16 only, and not with MOE_OPT_SHARED_FOLD, where 2
+   * is used instead). MX layers use their own kernels whatever the value. */
   MOE_OPT_GEMM_MODE = 0,
   /* 1 = record CUDA events between the stages of moe_layer_forward so
    * moe_read_stage_times can report per-stage device time. Default 0. */
@@ -124,7 +128,14 @@ typedef enum {
    * instead of on the side stream (bf16 layers with I_shared == I and
    * E <= 1023; otherwise ignored). The result is the same; which is faster
    * depends on the shape. Default 0 (side stream). */
-  MOE_OPT_SHARED_FOLD = 3
+  MOE_OPT_SHARED_FOLD = 3,
+  /* SMs given to the shared expert while it runs on the side stream; the
+   * routed GEMMs' persistent grids take the rest. 0 = no split (default):
+   * both streams' GEMMs size their grids to every SM, and the shared
+   * kernels fill the SMs that routing and permutation leave idle (no fixed
+   * split measured faster on the decode, MX, skewed or prefill workloads).
+   * k > 0 = k SMs (at most half). The result is the same either way. */
+  MOE_OPT_SHARED_SMS = 4
 } moe_option_t;
 
 /* Stage indices reported by moe_read_stage_times. */

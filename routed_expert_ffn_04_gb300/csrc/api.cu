@@ -37,6 +37,7 @@ struct moe_handle {
   int gemm_mode = kModeAuto;
   int stage_timing = 0;
   int shared_fold = 0;  // MOE_OPT_SHARED_FOLD
+  int shared_sms = 0;   // MOE_OPT_SHARED_SMS: 0 no split, k > 0 fixed
   uint64_t wait_limit_ns = kDefaultWaitLimitNs;
   cudaEvent_t* tev = nullptr;  // [kTimingRing][kEventsPerCall], created on first use
   int t_calls = 0;             // calls recorded since the last read
@@ -80,6 +81,17 @@ moe_status_t check_cfg(const moe_config_t* c) {
 // (MOE_OPT_SHARED_FOLD): bf16, the same intermediate size, a group to spare.
 bool foldable(const moe_config_t* c) {
   return c->dtype == MOE_BF16 && c->I_shared > 0 && c->I_shared == c->I && c->E + 1 <= 1024;
+}
+
+// SMs the shared expert gets while it runs beside the routed path on the side
+// stream (0: no split, the default). Measured on the decode, MX, skewed and
+// prefill workloads, no fixed split beat letting both streams' persistent
+// grids take every SM: the shared kernels then fill the SMs that the short
+// routing and permutation stages leave idle.
+int shared_sm_budget(int num_sms, int option) {
+  if (option <= 0 || num_sms < 4) return 0;
+  const int cap = num_sms / 2;
+  return option < cap ? option : cap;
 }
 
 // Workspace layout of moe_layer_forward, every piece 256-byte aligned.
@@ -280,7 +292,7 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
   if (!h) return MOE_ERR_INVALID_ARG;
   switch (opt) {
     case MOE_OPT_GEMM_MODE:
-      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 3) return MOE_ERR_INVALID_ARG;
       h->gemm_mode = value;
       return MOE_OK;
     case MOE_OPT_STAGE_TIMING:
@@ -293,6 +305,10 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
       return MOE_OK;
     case MOE_OPT_SHARED_FOLD:
       h->shared_fold = value ? 1 : 0;
+      return MOE_OK;
+    case MOE_OPT_SHARED_SMS:
+      if (value < 0) return MOE_ERR_INVALID_ARG;
+      h->shared_sms = value;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -566,6 +582,9 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   // Folded: the shared expert is group E of the routed GEMMs (rows TK..TK+T-1
   // of x_perm, h and y_perm), so nothing runs on the side stream.
   const bool fold = h->shared_fold && foldable(cfg);
+  // Optionally the shared expert's GEMMs get a few SMs of their own and the
+  // routed GEMMs the rest (MOE_OPT_SHARED_SMS; off by default).
+  const int k_sh = (has_shared && !fold && ss) ? shared_sm_budget(h->num_sms, h->shared_sms) : 0;
   if (has_shared && !fold) {
     if (ss) {
       e = cudaEventRecord(h->ev_in, sm);  // input ready on main
@@ -579,6 +598,7 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     // use few SMs well: up to 128 tokens its weights fill the MMA rows
     // (more CTAs stream them) unless a tiling is forced.
     if (!mx && g.mode == kModeAuto && T <= 128) g.mode = kModeWeightsM;
+    if (k_sh > 0) g.num_sms = k_sh;
     if (mx) {
       g.a_scale = at<uint8_t>(ws, L.x_mx_atoms);
       g.h_scale = at<uint8_t>(ws, L.h_shared_s);
@@ -616,6 +636,7 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
                                 w->w_gate, w->w_up, w->w_down, hbuf, y_perm,
                                 mx ? w->s_gate : nullptr, mx ? w->s_down : nullptr);
   g.w4 = w4;
+  if (k_sh > 0) g.num_sms = h->num_sms - k_sh;
   if (fold) {
     g.shared_w_gate = w->ws_gate;
     g.shared_w_up = w->ws_up;

@@ -580,6 +580,10 @@ bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t out
   return make_map_f32(m, ptr, inner, outer);
 }
 
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  return make_map(m, ptr, false, inner, outer, box_rows);
+}
+
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
   return make_map(m, ptr, true, inner, outer, box_rows);
 }
@@ -663,15 +667,26 @@ cudaError_t set_smem_attribute() {
 }
 
 int pick_mode(const GroupedGemmArgs& a) {
-  if (a.mode == kModeWeightsM || a.mode == kModeTokensM) return a.mode;
-  const int G = a.offsets ? a.G : 1;
-  const double avg_rows = (double)a.rows / (G > 0 ? G : 1);
-  return avg_rows <= 48.0 ? kModeWeightsM : kModeTokensM;
+  int m = a.mode;
+  if (m != kModeWeightsM && m != kModeTokensM && m != kModePair) {
+    const int G = a.offsets ? a.G : 1;
+    const double avg_rows = (double)a.rows / (G > 0 ? G : 1);
+    m = avg_rows <= 48.0 ? kModeWeightsM : kModeTokensM;
+  }
+  if (m == kModePair && !gemm_pair_supported(a)) m = kModeTokensM;
+  return m;
 }
 
 template <int MODE>
 cudaError_t launch_mode(const GroupedGemmArgs& a, cudaStream_t s) {
-  return pick_mode(a) == kModeWeightsM ? run_gemm<true, MODE, 32>(a, s) : run_gemm<false, MODE, 32>(a, s);
+  switch (pick_mode(a)) {
+    case kModeWeightsM:
+      return run_gemm<true, MODE, 32>(a, s);
+    case kModePair:
+      return MODE == 0 ? launch_gemm_pair_gate_up(a, s) : launch_gemm_pair_down(a, s);
+    default:
+      return run_gemm<false, MODE, 32>(a, s);
+  }
 }
 
 }  // namespace
@@ -692,7 +707,7 @@ cudaError_t gemm_prepare_device() {
   const cudaError_t errs[] = {
       set_smem_attribute<true, 0, 32>(), set_smem_attribute<false, 0, 32>(),
       set_smem_attribute<true, 1, 32>(), set_smem_attribute<false, 1, 32>(),
-      set_smem_attribute<false, 2, 32>()};
+      set_smem_attribute<false, 2, 32>(), gemm_pair_prepare_device()};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;

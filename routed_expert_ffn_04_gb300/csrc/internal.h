@@ -50,7 +50,9 @@ cudaError_t launch_scatter_rows(const void* src, int T, int row_bytes, const int
                                 int K, int TK, void* dst, int* status, cudaStream_t s);
 
 // ---- grouped GEMM (gemm.cu)
-enum GemmMode { kModeAuto = 0, kModeWeightsM = 1, kModeTokensM = 2 };
+// kModePair: weights as the M = 256 rows of an MMA spread over a CTA pair
+// (gemm_pair.cu), tokens as N.
+enum GemmMode { kModeAuto = 0, kModeWeightsM = 1, kModeTokensM = 2, kModePair = 3 };
 
 struct GroupedGemmArgs {
   int G;                   // number of groups
@@ -93,6 +95,8 @@ cudaError_t gemm_prepare_device();
 // 2-D fp32 tensor map [outer, inner] for bulk stores of 32 x 32 blocks from a
 // 128-byte-swizzled shared-memory buffer (inner % 32 == 0).
 bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer);
+// 2-D bf16 tensor map [outer, inner], box {64 elements, box_rows}, 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
 // 2-D uint8 tensor map [outer, inner], box {128 bytes, box_rows}, 128-byte swizzle.
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
 // 2-D packed E2M1 tensor map [outer, inner elements] (inner / 2 bytes per row;
@@ -108,6 +112,11 @@ cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
+// CTA-pair bf16 grouped GEMM (gemm_pair.cu); not for a folded shared expert.
+bool gemm_pair_supported(const GroupedGemmArgs& a);
+cudaError_t gemm_pair_prepare_device();
+cudaError_t launch_gemm_pair_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_pair_down(const GroupedGemmArgs& a, cudaStream_t s);
 // Gating GEMM (one group, E <= 256) with routing in its epilogue: a.h = x
 // [rows, a.I], a.w_down = router weights [a.H = E, a.I], a.y = logits out
 // (nullable), routing into a.topk_idx / a.topk_w.

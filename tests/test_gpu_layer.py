@@ -187,3 +187,19 @@ def test_bounded_wait_times_out_and_reports(handle):
         check_layer(out, ref, what="after timeout")
     finally:
         handle.set_option(moe.MOE_OPT_WAIT_LIMIT_US, 2_000_000)
+
+
+def test_shared_sm_split_does_not_change_the_result(handle):
+    # MOE_OPT_SHARED_SMS only sizes the persistent grids of the two streams'
+    # GEMMs; every row's arithmetic is the same, so the output is bit-identical.
+    shape = synth.MoEShape("split", T=300, H=512, E=32, K=4, I=256, I_shared=256)
+    x, logits, w = make_problem(shape, seed=11)
+    outs = []
+    for k in (0, 2, 3, 1000):
+        handle.set_option(moe.MOE_OPT_SHARED_SMS, k)
+        outs.append(run_layer(handle, shape, x, logits, w).clone())
+    handle.set_option(moe.MOE_OPT_SHARED_SMS, 0)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    with pytest.raises(moe.MoEError):
+        handle.set_option(moe.MOE_OPT_SHARED_SMS, -1)
