@@ -68,7 +68,7 @@ struct Geo {
   static constexpr int ACC_COLS = SWAP ? 2 * BN : 256;               // TMEM cols / buffer
   static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32) ? 32 : (2 * ACC_COLS <= 64) ? 64
                                    : (2 * ACC_COLS <= 128) ? 128 : (2 * ACC_COLS <= 256) ? 256 : 512;
-  static constexpr int TABLE_BYTES = (kMaxGroups + 8) * 4;
+  static constexpr int TABLE_BYTES = 2 * (kMaxGroups + 8) * 4;  // tile starts, row starts
   static constexpr int BAR_BYTES = 512;
   // Tokens-as-M epilogue: a per-warp 32 x 32 fp32 staging block. GEMM-2 stores
   // it by TMA (4 KB, 128-byte swizzled, 1024-aligned: 5 KB per warp, which also
@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
   // Shared memory: ring | epilogue staging (1024-aligned) | tile table | barriers.
   float* epi_stage = reinterpret_cast<float*>(base + Gm::RING_BYTES);
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + Gm::RING_BYTES + Gm::EPI_BYTES);
+  int32_t* row_start = tile_start + kMaxGroups + 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::RING_BYTES + Gm::EPI_BYTES + Gm::TABLE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Gm::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -334,13 +335,14 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- tile table: tile_start[g] = tiles of groups before g.
+  // ---- tile table: tile_start[g] = tiles of groups before g; row starts.
   const int n_wt = (p.N + Gm::W_COLS - 1) / Gm::W_COLS;
   for (int g = threadIdx.x; g < p.G; g += Gm::THREADS) {
     int r0, nr;
     group_rows(p, g, r0, nr);
     tile_start[g] = n_wt * ((nr + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS);
   }
+  fill_row_start(p, row_start, threadIdx.x, Gm::THREADS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full_bar(s), 1);
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
       Armed armed;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<Gm::ACT_ROWS>(p, tile_start, tile);
+        const TileInfo ti = decode_tile_s<Gm::ACT_ROWS>(p.G, tile_start, row_start, tile);
         const int act_row = ti.row0 + ti.tt * Gm::ACT_ROWS;
         const bool shg = ti.g == p.fold_group;  // the folded shared expert's group
         const CUtensorMap* mw0 = shg ? &map_w0s : &map_w0;
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const TileInfo ti = decode_tile<Gm::ACT_ROWS>(p, tile_start, tile);
+      const TileInfo ti = decode_tile_s<Gm::ACT_ROWS>(p.G, tile_start, row_start, tile);
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Gm::ACC_COLS);
       epilogue_tile<SWAP, MODE, BN>(p, ti, tb, q, lane, epi_stage + q * (Gm::EPI_WARP / 4), &map_y);
       tc_fence_before();

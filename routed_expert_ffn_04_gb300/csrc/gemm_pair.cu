@@ -28,12 +28,12 @@
 // from the odd's). One MMA per 16-wide K step keeps the single issuing thread
 // ahead of the tensor pipe.
 //
-// Roles in each CTA (192 threads): warp 0 lane 0 loads both CTAs' halves by
-// TMA into local stages (local full barriers); warp 1 lane 0 of the even CTA
-// (leader) waits for its own stage and for the odd CTA's report that its half
-// has landed, then issues the pair MMAs and commits to both CTAs' empty and
-// accumulator barriers; warp 1 lane 0 of the odd CTA relays its full stages
-// to the leader; warps 2-5 of both CTAs read their TMEM lanes and store h / y,
+// Roles in each CTA (192 threads): warp 0 lane 0 of each CTA loads its
+// halves by TMA into local stages (local full barriers); warp 1 lane 0 of the
+// odd CTA relays each landed stage to the leader's full barrier for that
+// stage, which therefore completes once both halves are in; warp 1 lane 0 of
+// the even CTA (leader) waits on it, issues the pair MMAs and commits to both
+// CTAs' empty and accumulator barriers; warps 2-5 of both CTAs read their TMEM lanes and store h / y,
 // then tell the leader the accumulator is free. All waits are bounded (about
 // 2 s): on expiry the CTA records an error code, raises its abort flag,
 // drains its in-flight copies (the leader its MMAs), and both CTAs meet at a
@@ -50,7 +50,8 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 64;           // K elements per stage: one 128-byte swizzle row of bf16
+constexpr int kBK = 64;           // K elements per sub-tile: one 128-byte swizzle row of bf16
+constexpr int kKSub = 2;          // sub-tiles per stage: 128 K elements per stage
 constexpr int kMaxGroups = 1024;
 constexpr int kMaxSmem = 232448;  // 227 KB dynamic shared memory per CTA
 constexpr uint16_t kPairMask = 0x3;
@@ -60,17 +61,18 @@ struct PairGeo {
   static constexpr int W_ROWS = 128;                  // weight rows per CTA (half of M = 256)
   static constexpr int F_CTA = MODE == 0 ? 64 : 128;  // output features per CTA
   static constexpr int W_COLS = 2 * F_CTA;            // output features per pair tile
-  static constexpr int NA = 1;                        // A tiles per stage
   static constexpr int NT = 256;                      // tokens per pair tile at most (N)
   static constexpr int B_ROWS = NT / 2;               // token rows each CTA stages
-  static constexpr int A_BYTES = W_ROWS * 128;        // 16 KB
-  static constexpr int B_BYTES = B_ROWS * 128;
-  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = W_ROWS * 128;        // 16 KB: one A sub-tile
+  static constexpr int B_BYTES = B_ROWS * 128;        // 16 KB: one B sub-tile
+  static constexpr int STAGE_BYTES = kKSub * (A_BYTES + B_BYTES);
   static constexpr int ACC_COLS = NT;                 // TMEM columns per accumulator buffer
   static constexpr int W_BOX = MODE == 0 ? 16 : 128;  // rows per weight TMA box
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 192;
-  static constexpr int TABLE_BYTES = (kMaxGroups + 8) * 4;
+  // GEMM-1 stages 16 weight boxes per stage; a second producer warp (warp 6)
+  // issues the up boxes so that TMA issue keeps pace with the MMAs.
+  static constexpr int THREADS = MODE == 0 ? 224 : 192;
+  static constexpr int TABLE_BYTES = 2 * (kMaxGroups + 8) * 4;  // tile starts, row starts
   static constexpr int BAR_BYTES = 512;
   // Shared memory: the A tiles of every stage, then the B tiles of every
   // stage, then the tile table and barriers, then SLACK unused bytes. Each
@@ -80,25 +82,31 @@ struct PairGeo {
   static constexpr int EXTRA = 1024 + TABLE_BYTES + BAR_BYTES + SLACK;
   static constexpr int S_FREE = (kMaxSmem - EXTRA) / STAGE_BYTES;
   static constexpr int S = S_FREE > 8 ? 8 : S_FREE;
-  static constexpr int A_REGION = S * NA * A_BYTES;
+  static constexpr int A_REGION = S * kKSub * A_BYTES;
   static constexpr int RING_BYTES = S * STAGE_BYTES;
   static constexpr int SMEM = EXTRA + RING_BYTES;
   static_assert(SLACK >= B_BYTES && SLACK >= A_BYTES, "slack covers a doubled read");
-  static constexpr int NBARS = 3 * S + 5;  // full, pfull, empty [S]; tfull[2], tempty[2], drain
+  static constexpr int NBARS = 2 * S + 5;  // full, empty [S]; tfull[2], tempty[2], drain
   static_assert(S >= 3, "ring too shallow");
+  static_assert(A_REGION + S * kKSub * B_BYTES == RING_BYTES, "ring layout");
   static_assert(2 * ACC_COLS <= TMEM_COLS, "two accumulator buffers");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte alignment of swizzled tiles");
   static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM <= kMaxSmem, "shared memory budget");
 };
 
-// Tokens of the tile's chunk and the MMA's N (the chunk rounded up to 32, so
-// each CTA's half is a multiple of 16 rows).
+// Tokens of the tile's chunk and the MMA's N. A group of r rows is cut into
+// ceil(r / NT) chunks of one size (r / chunks rounded up to 32, so each CTA's
+// half is a multiple of 16 rows), the last taking the rest: 341 rows give
+// 192 + 149 rather than 256 + 85, so neither chunk leaves the tensor pipe
+// waiting on the issuing thread. N is the chunk rounded up to 32.
 template <int NT>
 __device__ __forceinline__ void chunk_of(const TileInfo& ti, int& tok0, int& ntok, int& n) {
-  tok0 = ti.tt * NT;
+  const int chunks = (ti.nrows + NT - 1) / NT;
+  const int cs = ((ti.nrows + chunks - 1) / chunks + 31) & ~31;
+  tok0 = ti.tt * cs;
   const int left = ti.nrows - tok0;
-  ntok = left < NT ? left : NT;
+  ntok = left < cs ? left : cs;
   n = (ntok + 31) & ~31;
 }
 
@@ -173,16 +181,19 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
   // abort flag | slack. The layout is the same in both CTAs, so a
   // descriptor's offsets address the matching half in the peer.
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + Gm::RING_BYTES);
+  int32_t* row_start = tile_start + kMaxGroups + 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::RING_BYTES + Gm::TABLE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Gm::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
+  // full[s]: in the leader two arrivals (its producer's, with the stage's
+  // bytes, and the peer's relay once the peer's half has landed); in the
+  // peer one (its producer's).
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto pfull_bar = [&](int s) { return bar0 + 8u * (NS + s); };   // leader: the peer's half landed
-  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * NS + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * NS + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * NS + 2 + a); };  // leader: 8 epilogue warps
-  const uint32_t drain_bar = bar0 + 8u * (3 * NS + 4);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NS + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NS + 2 + a); };  // leader: 8 epilogue warps
+  const uint32_t drain_bar = bar0 + 8u * (2 * NS + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
@@ -195,10 +206,10 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
     group_rows(p, g, r0, nr);
     tile_start[g] = n_wt * ((nr + Gm::NT - 1) / Gm::NT);
   }
+  fill_row_start(p, row_start, threadIdx.x, Gm::THREADS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(pfull_bar(s), 1);
+      mbar_init(full_bar(s), rank == 0 ? 2 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -254,36 +265,38 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
       Ring rg;
       Armed armed;
       bool ok = true;
+      const int n_stages = (p.num_kb + kKSub - 1) / kKSub;
       for (int tile = pair; ok && tile < total; tile += npairs) {
-        const TileInfo ti = decode_tile<Gm::NT>(p, tile_start, tile);
+        const TileInfo ti = decode_tile_s<Gm::NT>(p.G, tile_start, row_start, tile);
         int tok0, ntok, n;
         chunk_of<Gm::NT>(ti, tok0, ntok, n);
         const int act_row = ti.row0 + tok0 + (int)rank * (n / 2);
         // First weight row of this CTA's A tile: GEMM-1 the gate and up rows of
         // 64 features, GEMM-2 128 rows of W_down.
         const int w_row = ti.g * p.N + ti.wt * Gm::W_COLS + (int)rank * Gm::F_CTA;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < n_stages; ++kb) {
           if (!mbar_wait_bounded_cluster(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
                                          MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns)) {
             ok = false;
             break;
           }
-          const int kx = kb * kBK;
+          const int nsub = p.num_kb - kb * kKSub < kKSub ? p.num_kb - kb * kKSub : kKSub;
           const uint32_t fb = full_bar(rg.s);
-          mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-          const uint32_t sA = base_u32 + rg.s * Gm::NA * Gm::A_BYTES;
-          if (MODE == 0) {
-            // Quarter t of the A tile (32 rows, 4 KB): gate rows of features
-            // 16t .. 16t+15, then their up rows.
+          mbar_arrive_expect_tx(fb, (uint32_t)nsub * (Gm::A_BYTES + Gm::B_BYTES));
+          for (int j = 0; j < nsub; ++j) {
+            const int kx = (kb * kKSub + j) * kBK;
+            const uint32_t sA = base_u32 + (rg.s * kKSub + j) * Gm::A_BYTES;
+            if (MODE == 0) {
+              // Quarter t of the A sub-tile (32 rows, 4 KB): gate rows of
+              // features 16t .. 16t+15, then their up rows (warp 6 loads those).
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              tma_load_2d(sA + t * 4096, &map_w0, fb, kx, w_row + 16 * t);
-              tma_load_2d(sA + t * 4096 + 2048, &map_w1, fb, kx, w_row + 16 * t);
+              for (int t = 0; t < 4; ++t) tma_load_2d(sA + t * 4096, &map_w0, fb, kx, w_row + 16 * t);
+            } else {
+              tma_load_2d(sA, &map_w0, fb, kx, w_row);
             }
-          } else {
-            tma_load_2d(sA, &map_w0, fb, kx, w_row);
+            tma_load_2d(base_u32 + Gm::A_REGION + (rg.s * kKSub + j) * Gm::B_BYTES, &map_act, fb, kx,
+                        act_row);
           }
-          tma_load_2d(base_u32 + Gm::A_REGION + rg.s * Gm::B_BYTES, &map_act, fb, kx, act_row);
           armed.mark(rg);
           rg.next(NS);
         }
@@ -294,52 +307,69 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp walks the loop in step, so tile, stage and descriptor
+      // values are warp-uniform; lane 0 polls the barriers (the result is
+      // broadcast) and issues the tcgen05 instructions.
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        int v = 0;
+        if (lane == 0)
+          v = mbar_wait_bounded_cluster(bar, parity, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
+                                        p.limit_ns) ? 1 : 0;
+        return __shfl_sync(0xFFFFFFFFu, v, 0) != 0;
+      };
       Ring rg;
       bool ok = true, issued = false;
       int local = 0;
+      const int n_stages = (p.num_kb + kKSub - 1) / kKSub;
       for (int tile = pair; ok && tile < total; tile += npairs, ++local) {
-        const TileInfo ti = decode_tile<Gm::NT>(p, tile_start, tile);
+        const TileInfo ti = decode_tile_s<Gm::NT>(p.G, tile_start, row_start, tile);
         int tok0, ntok, n;
         chunk_of<Gm::NT>(ti, tok0, ntok, n);
         const uint32_t idesc = idesc_bf16_f32(256, n);
         const int acc = local & 1;
         const uint32_t ap = (uint32_t)(local >> 1) & 1u;
-        if (!mbar_wait_bounded_cluster(tempty_bar(acc), ap ^ 1u, abort_flag, p.status,
-                                       MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+        if (!wait_all(tempty_bar(acc), ap ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * Gm::ACC_COLS);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait_bounded(full_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
-                                 p.limit_ns) ||
-              !mbar_wait_bounded_cluster(pfull_bar(rg.s), rg.ph, abort_flag, p.status,
-                                         MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+        for (int kb = 0; kb < n_stages; ++kb) {
+          // Both halves of the stage: the leader's bytes and the peer's relay.
+          if (!wait_all(full_bar(rg.s), rg.ph)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sA = base_u32 + rg.s * Gm::NA * Gm::A_BYTES;
-          const uint32_t sB = base_u32 + Gm::A_REGION + rg.s * Gm::B_BYTES;
+          const int nsub = p.num_kb - kb * kKSub < kKSub ? p.num_kb - kb * kKSub : kKSub;
+          // Descriptors of the stage's first 16-wide K step; each further step
+          // is 32 bytes on (+2 in the start-address field), the second
+          // sub-tile 16 KB on (+1024).
+          const uint64_t a0 = sw128_kmajor_desc(base_u32 + rg.s * kKSub * Gm::A_BYTES);
+          const uint64_t b0 = sw128_kmajor_desc(base_u32 + Gm::A_REGION + rg.s * kKSub * Gm::B_BYTES);
+          if (lane == 0) {
+            for (int j = 0; j < nsub; ++j) {
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint32_t accum = (kb | k) ? 1u : 0u;
-            const uint64_t bdesc = sw128_kmajor_desc(sB + k * 32);
-            umma_bf16_pair(d, sw128_kmajor_desc(sA + k * 32), bdesc, idesc, accum);
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_bf16_pair(d, a0 + (uint64_t)(j * (Gm::A_BYTES >> 4) + 2 * k),
+                               b0 + (uint64_t)(j * (Gm::B_BYTES >> 4) + 2 * k), idesc,
+                               (kb | j | k) ? 1u : 0u);
+            }
+            umma_commit_pair_mc(empty_bar(rg.s), kPairMask);
           }
+          __syncwarp();
           issued = true;
-          umma_commit_pair_mc(empty_bar(rg.s), kPairMask);
           rg.next(NS);
         }
         if (!ok) break;
-        umma_commit_pair_mc(tfull_bar(acc), kPairMask);
+        if (lane == 0) umma_commit_pair_mc(tfull_bar(acc), kPairMask);
+        __syncwarp();
       }
       // Every MMA reads both CTAs' shared memory and writes both TMEMs: all
       // of them complete before either CTA goes on to leave.
-      if (issued) {
+      if (issued && lane == 0) {
         umma_commit_pair(drain_bar);
         drain_wait(drain_bar, 0, 200000000ull);
       }
@@ -348,16 +378,51 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
       // Report each landed stage of this CTA's half to the leader's MMA thread.
       Ring rg;
       bool ok = true;
+      const int n_stages = (p.num_kb + kKSub - 1) / kKSub;
       for (int tile = pair; ok && tile < total; tile += npairs) {
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < n_stages; ++kb) {
           if (!mbar_wait_bounded(full_bar(rg.s), rg.ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA,
                                  p.limit_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_remote(mapa_shared(pfull_bar(rg.s), 0));
+          mbar_arrive_remote(mapa_shared(full_bar(rg.s), 0));
           rg.next(NS);
         }
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ up boxes (GEMM-1)
+    if (MODE == 0 && lane == 0) {
+      Ring rg;
+      Armed armed;
+      bool ok = true;
+      const int n_stages = (p.num_kb + kKSub - 1) / kKSub;
+      for (int tile = pair; ok && tile < total; tile += npairs) {
+        const TileInfo ti = decode_tile_s<Gm::NT>(p.G, tile_start, row_start, tile);
+        const int w_row = ti.g * p.N + ti.wt * Gm::W_COLS + (int)rank * Gm::F_CTA;
+        for (int kb = 0; kb < n_stages; ++kb) {
+          if (!mbar_wait_bounded_cluster(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
+                                         MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          const int nsub = p.num_kb - kb * kKSub < kKSub ? p.num_kb - kb * kKSub : kKSub;
+          const uint32_t fb = full_bar(rg.s);  // bytes counted by warp 0's expect_tx
+          for (int j = 0; j < nsub; ++j) {
+            const int kx = (kb * kKSub + j) * kBK;
+            const uint32_t sA = base_u32 + (rg.s * kKSub + j) * Gm::A_BYTES;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              tma_load_2d(sA + t * 4096 + 2048, &map_w1, fb, kx, w_row + 16 * t);
+          }
+          armed.mark(rg);
+          rg.next(NS);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < NS; ++s)
+          if (armed.mask & (1u << s)) drain_wait(full_bar(s), (armed.phase >> s) & 1u, 100000000ull);
       }
     }
   } else {
@@ -374,7 +439,7 @@ __global__ void __launch_bounds__(PairGeo<MODE>::THREADS, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const TileInfo ti = decode_tile<Gm::NT>(p, tile_start, tile);
+      const TileInfo ti = decode_tile_s<Gm::NT>(p.G, tile_start, row_start, tile);
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Gm::ACC_COLS);
       epilogue_pair<MODE>(p, ti, tb, q, lane, rank);
       tc_fence_before();

@@ -71,6 +71,40 @@ __device__ __forceinline__ TileInfo decode_tile(const KParams& p, const int32_t*
   return t;
 }
 
+// The same decode from a shared-memory copy of the group starts
+// (row_start[g] = offsets[g] clamped to [0, rows], g = 0..G; see
+// fill_row_start), so that a role starting a tile does not wait on a global
+// load of the offsets.
+template <int ACT_ROWS>
+__device__ __forceinline__ TileInfo decode_tile_s(int G, const int32_t* tile_start,
+                                                  const int32_t* row_start, int tile) {
+  int lo = 0, hi = G;  // tile_start[lo] <= tile < tile_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo t;
+  t.g = lo;
+  t.row0 = row_start[lo];
+  const int nr = row_start[lo + 1] - t.row0;
+  t.nrows = nr > 0 ? nr : 0;
+  const int n_tt = (t.nrows + ACT_ROWS - 1) / ACT_ROWS;
+  const int local = tile - tile_start[lo];
+  t.wt = local / n_tt;
+  t.tt = local - t.wt * n_tt;
+  return t;
+}
+
+// row_start[g] for g = 0..G (executed by all `nthreads` threads of the CTA
+// before a __syncthreads): rows [row_start[g], row_start[g+1]) are group g,
+// as group_rows clamps them.
+__device__ __forceinline__ void fill_row_start(const KParams& p, int32_t* row_start, int tid, int nthreads) {
+  for (int g = tid; g <= p.G; g += nthreads) {
+    int v = p.offsets ? __ldg(p.offsets + g) : (g == 0 ? 0 : p.rows);
+    row_start[g] = v < 0 ? 0 : (v > p.rows ? p.rows : v);
+  }
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // Bounded wait that ignores the abort flag, used only to drain in-flight work.
