@@ -362,10 +362,11 @@ MOE_API moe_status_t moe_read_stage_times(moe_handle_t h, float* ms, int* n_call
  * cudaMalloc and have no workspace to hand over, such as a plugin inside an
  * engine that owns every device allocation, or code that must not allocate
  * after start-up).
- * Same arguments, results and kernels as moe_permute, minus ws/ws_bytes: the
- * per-warp histogram lives in a fixed array in the library's own device
- * memory, MOE_PERMUTE_STATIC_MAX_HIST_INTS int32 (1 MiB), which every GPU
- * that loads the library holds until the process exits.
+ * Same arguments, results and kernels as moe_permute, minus ws/ws_bytes. Up
+ * to 262144 (token, slot) pairs the permutation needs no scratch at all;
+ * above that the per-warp histogram lives in a fixed array in the library's
+ * own device memory, MOE_PERMUTE_STATIC_MAX_HIST_INTS int32 (1 MiB), which
+ * every GPU that loads the library holds until the process exits.
  * Limit: E * ceil(T*K / 256) <= MOE_PERMUTE_STATIC_MAX_HIST_INTS (for E = 192
  * and K = 8: T <= 43690); larger sizes return MOE_ERR_WORKSPACE before any
  * launch.

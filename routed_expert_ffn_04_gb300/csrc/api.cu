@@ -96,7 +96,7 @@ int shared_sm_budget(int num_sms, int option) {
 
 // Workspace layout of moe_layer_forward, every piece 256-byte aligned.
 struct Layout {
-  size_t topk_idx, topk_w, counts, offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
+  size_t topk_idx, topk_w, counts, offsets, tile_offsets, perm_src, flat_to_perm, perm_scratch, x_perm, h,
       y_perm, s, h_shared, x_stage, logits_stage, out_stage, x_mx, total;
   // MXFP8 only: E8M0 scales of x (x_mx holds its E4M3 codes) row-major and
   // as scale atoms; atoms of the permuted x, of h and of the shared expert's h.
@@ -116,6 +116,7 @@ Layout layout_of(const moe_config_t* c) {
   L.topk_w = take(TK * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 2) * 4);  // + the folded shared group's end
+  L.tile_offsets = take((E + 1) * 4);
   L.perm_src = take(TK * 4);
   L.flat_to_perm = take(TK * 4);
   L.perm_scratch = take(permute_scratch_bytes((int)TK, (int)E));
@@ -261,6 +262,7 @@ MOE_API moe_status_t moe_create(int device, moe_handle_t* out) {
   h->device = device;
   h->num_sms = sms;
   if (gemm_prepare_device() != cudaSuccess || gemm_mx_prepare_device() != cudaSuccess ||
+      permute_prepare_device() != cudaSuccess ||
       gate_small_prepare_device() != cudaSuccess ||
       cudaMalloc(&h->status, 64) != cudaSuccess ||
       cudaMemset(h->status, 0, 64) != cudaSuccess ||
@@ -361,8 +363,8 @@ MOE_API moe_status_t moe_permute(moe_handle_t h, const moe_config_t* cfg, const 
   if ((st = check_handle(h)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int TK = cfg->T * cfg->K;
-  cudaError_t e = launch_permute_index(topk_idx, TK, cfg->E, ws, counts, offsets, perm_src,
-                                       flat_to_perm, h->status, s);
+  cudaError_t e = launch_permute_index(topk_idx, TK, cfg->E, ws, counts, offsets, nullptr,
+                                       perm_src, flat_to_perm, h->status, s);
   if (e == cudaSuccess)
     e = launch_scatter_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, flat_to_perm, cfg->K, TK, x_perm,
                             h->status, s);
@@ -616,14 +618,17 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
       e = launch_route(logits, T, E, K, cfg->scaling, cfg->route_norm, topk_idx, topk_w, sm);
     mark(1, sm);
   }
+  int32_t* tile_offsets = mx ? at<int32_t>(ws, L.tile_offsets) : nullptr;
   if (e == cudaSuccess)
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
-                             perm_src, flat_to_perm, h->status, sm);
+                             tile_offsets, perm_src, flat_to_perm, h->status, sm);
+  // MX: the E4M3 rows and their scale atoms in one pass; bf16: the rows.
   if (e == cudaSuccess)
-    e = launch_scatter_rows(x, T, mx ? H : H * 2, flat_to_perm, K, TK, x_perm, h->status, sm);
-  if (e == cudaSuccess && mx)
-    e = launch_gather_scale_atoms(xq_s, T, H, perm_src, K, offsets, E, TK,
-                                  at<uint8_t>(ws, L.x_perm_s), h->status, sm);
+    e = mx ? launch_scatter_rows_mx(static_cast<const uint8_t*>(x), xq_s, T, H, flat_to_perm,
+                                    topk_idx, offsets, tile_offsets, K, TK, E,
+                                    static_cast<uint8_t*>(x_perm), at<uint8_t>(ws, L.x_perm_s),
+                                    h->status, sm)
+           : launch_scatter_rows(x, T, H * 2, flat_to_perm, K, TK, x_perm, h->status, sm);
   if (e == cudaSuccess && fold) {  // group E: x itself, after the routed rows
     set_i32_kernel<<<1, 1, 0, sm>>>(offsets + E + 1, TK + T);
     e = cudaGetLastError();

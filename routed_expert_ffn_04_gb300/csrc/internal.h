@@ -39,15 +39,29 @@ cudaError_t launch_gate_route_small(const void* x, const void* w_router, int T, 
 
 // ---- permutation (permute.cu)
 size_t permute_scratch_bytes(int TK, int E);
+// Opt the cluster permutation into its dynamic shared memory (once per device).
+cudaError_t permute_prepare_device();
+// counts [E], offsets [E+1], perm_src / flat_to_perm [TK]; tile_offsets
+// (nullable) [E+1]: the first 128-row tile of each expert. scratch is used
+// only above the single-launch sizes (more than 262144 pairs).
 cudaError_t launch_permute_index(const int32_t* topk_idx, int TK, int E, void* scratch,
-                                 int32_t* counts, int32_t* offsets, int32_t* perm_src,
-                                 int32_t* flat_to_perm, int* status, cudaStream_t s);
+                                 int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
+                                 int32_t* perm_src, int32_t* flat_to_perm, int* status,
+                                 cudaStream_t s);
 // dst[r, :] = src[perm_src[r] / K, :] for r < TK; rows are row_bytes long
 // (a multiple of 16). A perm_src entry outside [0, TK) gives a zero row.
 // x_perm[flat_to_perm[t*K+k]] = x[t] for every token t and slot k: each
 // source row read once (row_bytes a multiple of 4).
 cudaError_t launch_scatter_rows(const void* src, int T, int row_bytes, const int32_t* flat_to_perm,
                                 int K, int TK, void* dst, int* status, cudaStream_t s);
+// MX rows: x_q [T, H] E4M3 codes -> x_perm [TK, H], and the row-major scales
+// x_scale [T, H/32] into the scale atoms of the permuted rows (by expert tile,
+// tile_offsets from launch_permute_index). H % 128 == 0.
+cudaError_t launch_scatter_rows_mx(const uint8_t* x_q, const uint8_t* x_scale, int T, int H,
+                                   const int32_t* flat_to_perm, const int32_t* topk_idx,
+                                   const int32_t* offsets, const int32_t* tile_offsets, int K, int TK,
+                                   int E, uint8_t* x_perm, uint8_t* atoms, int* status,
+                                   cudaStream_t s);
 
 // ---- grouped GEMM (gemm.cu)
 // kModePair: weights as the M = 256 rows of an MMA spread over a CTA pair

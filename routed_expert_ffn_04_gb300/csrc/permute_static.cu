@@ -87,7 +87,7 @@ extern "C" MOE_API moe_status_t moe_permute_static_scratch(
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int TK = cfg->T * cfg->K;
   cudaError_t e = moe::launch_permute_index(topk_idx, TK, cfg->E, scratch, counts, offsets,
-                                            perm_src, flat_to_perm, status, s);
+                                            nullptr, perm_src, flat_to_perm, status, s);
   if (e == cudaSuccess)
     e = moe::launch_scatter_rows(x, cfg->T, mx ? cfg->H : cfg->H * 2, flat_to_perm, cfg->K, TK,
                                  x_perm, status, s);

@@ -314,6 +314,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
   return r;
 }
+// 32-bit load from the shared memory of a CTA of this cluster (address from
+// mapa_shared).
+__device__ __forceinline__ int32_t ld_shared_cluster_s32(uint32_t cluster_addr) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 // Arrive once, relaxed, on an mbarrier of another CTA of the cluster (address
 // from mapa_shared). Used only to announce work whose completion the caller
 // has already observed (a TMA stage's barrier phase, TMEM loads waited on and

@@ -96,9 +96,13 @@ PERM_CASES = {
     "ragged": synth.MoEShape("ragged", T=77, H=128, E=13, K=3, I=64, I_shared=0),
     "e1024": synth.MoEShape("e1024", T=300, H=64, E=1024, K=32, I=64, I_shared=0),
     "t1": synth.MoEShape("t1", T=1, H=64, E=8, K=2, I=64, I_shared=0),
-    # one-block counting sort up to 16384 pairs, three kernels above
-    "tk16384": synth.MoEShape("tk16384", T=2048, H=64, E=192, K=8, I=64, I_shared=0),
+    # one block up to 4096 pairs, a cluster of 8 blocks up to 262144, three kernels above
+    "tk4096": synth.MoEShape("tk4096", T=512, H=64, E=192, K=8, I=64, I_shared=0),
+    "tk4097": synth.MoEShape("tk4097", T=4097, H=64, E=37, K=1, I=64, I_shared=0),
     "tk16392": synth.MoEShape("tk16392", T=2049, H=64, E=192, K=8, I=64, I_shared=0),
+    "tk262144": synth.MoEShape("tk262144", T=32768, H=64, E=256, K=8, I=64, I_shared=0),
+    "tk262145": synth.MoEShape("tk262145", T=262145, H=64, E=64, K=1, I=64, I_shared=0),
+    "e1024_cluster": synth.MoEShape("e1024c", T=3000, H=64, E=1024, K=8, I=64, I_shared=0),
     "e1024_one_block": synth.MoEShape("e1024s", T=200, H=64, E=1024, K=32, I=64, I_shared=0),
 }
 

@@ -5,13 +5,14 @@ has started). Its histogram lives in a fixed array inside the library.
 
 The GPU test calls it through the C ABI on a sequence of shapes, each twice in
 a row, and checks every result against moe_permute with a caller workspace.
-The sequence covers both permutation paths: up to 16384 (token, slot) pairs
-one block keeps its counters in shared memory; above that the three-kernel
-path keeps its per-warp histogram in the fixed array, and the later shapes
-(another E, another number of warps) find the earlier shapes' entries still
-there. It also covers MXFP8 and W4A8 configs, whose rows are 1-byte E4M3
-codes with their E8M0 scales. The permutation is integer work, so the bar is
-bit-exact, as for moe_permute itself. This file is collected last so that a
+Up to 262144 (token, slot) pairs the permutation keeps its counters in
+shared memory (one block, or a cluster of eight); above that the three-kernel
+path keeps its per-warp histogram in the fixed array. The sequence covers
+both, and the later large shapes (another E, another number of warps) find
+the earlier ones' entries still in the array. It also covers MXFP8 and W4A8
+configs, whose rows are 1-byte E4M3 codes with their E8M0 scales. The
+permutation is integer work, so the bar is bit-exact, as for moe_permute
+itself. This file is collected last so that a
 run stopping at the first failure has run every other test."""
 import ctypes
 
@@ -22,16 +23,17 @@ import torch
 import routed_expert_ffn_04_gb300 as moe
 import synth
 
-# (shape, dtype name). T*K above 16384 takes the three-kernel path, the one
+# (shape, dtype name). T*K above 262144 takes the three-kernel path, the one
 # that uses the fixed array.
 CASES = [
-    (synth.WORKLOADS["decode"].with_(H=512, I=256, I_shared=256), "bf16"),                # 512 pairs
-    (synth.WORKLOADS["skewed"].with_(H=256, I=128, I_shared=128), "bf16"),                # 32768 pairs, E=256
-    (synth.MoEShape("ragged", T=2049, H=256, E=192, K=8, I=128, I_shared=0), "bf16"),      # 16392 pairs
-    (synth.MoEShape("ragged_e37", T=3333, H=256, E=37, K=5, I=128, I_shared=0), "bf16"),   # 16665 pairs
-    (synth.MoEShape("mx8", T=2049, H=512, E=192, K=8, I=128, I_shared=128), "mxfp8"),     # 16392 pairs
-    (synth.MoEShape("w4a8", T=2500, H=384, E=160, K=8, I=128, I_shared=128), "mxfp4"),    # 20000 pairs, H % 512 != 0
-    (synth.MoEShape("w4a8_small", T=333, H=384, E=37, K=5, I=128, I_shared=0), "mxfp4"),  # 1665 pairs
+    (synth.WORKLOADS["decode"].with_(H=512, I=256, I_shared=256), "bf16"),                 # 512 pairs
+    (synth.MoEShape("big_e64", T=40000, H=64, E=64, K=8, I=64, I_shared=0), "bf16"),        # 320000 pairs
+    (synth.MoEShape("big_e200", T=70001, H=64, E=200, K=4, I=64, I_shared=0), "bf16"),      # 280004 pairs
+    (synth.WORKLOADS["skewed"].with_(H=256, I=128, I_shared=128), "bf16"),                 # 32768 pairs, E=256
+    (synth.MoEShape("mx8_big", T=33000, H=128, E=64, K=8, I=128, I_shared=0), "mxfp8"),     # 264000 pairs
+    (synth.MoEShape("w4a8_big", T=90000, H=384, E=37, K=3, I=128, I_shared=0), "mxfp4"),    # 270000 pairs, H % 512 != 0
+    (synth.MoEShape("mx8", T=2049, H=512, E=192, K=8, I=128, I_shared=128), "mxfp8"),      # 16392 pairs
+    (synth.MoEShape("w4a8_small", T=333, H=384, E=37, K=5, I=128, I_shared=0), "mxfp4"),   # 1665 pairs
 ]
 
 
