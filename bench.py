@@ -67,6 +67,9 @@ def parse():
                     help="MOE_OPT_GEMM_MODE for the timed calls (0 automatic, 1 weights-as-M, 2 tokens-as-M, 3 CTA pair)")
     ap.add_argument("--ab-gemm-modes", default="",
                     help="comma-separated GEMM modes to time against each other (interleaved graph replays)")
+    ap.add_argument("--ab-option", default="",
+                    help="OPTION=v1,v2,...: time the layer with each value of a handle option (by number) "
+                         "against each other, as --ab-gemm-modes does")
     ap.add_argument("--shared-sms-sweep", default="",
                     help="comma-separated MOE_OPT_SHARED_SMS values to add to the overlap measurement")
     ap.add_argument("--experts", type=int, default=None,
@@ -327,18 +330,21 @@ def interleaved_replays(variants, main, dev, rounds=200):
     return times
 
 
-def measure_gemm_modes(moe, layer, modes, call, main, dev, rounds=200):
-    """The layer with each grouped-GEMM tiling: interleaved graph replays, and
-    per-stage device times from 30 eager calls each."""
+def measure_gemm_modes(moe, layer, modes, call, main, dev, rounds=200, option=None, restore=0):
+    """The layer with each value of a handle option (default: the grouped-GEMM
+    tiling): interleaved graph replays, and per-stage device times from 30
+    eager calls each."""
     import torch
 
+    opt = moe.MOE_OPT_GEMM_MODE if option is None else option
+
     def setter(m):
-        return lambda: layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, m)
+        return lambda: layer.handle.set_option(opt, m)
 
     times = interleaved_replays({f"mode{m}": (setter(m), call) for m in modes}, main, dev, rounds)
     stages = {}
     for m in modes:
-        layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, m)
+        layer.handle.set_option(opt, m)
         for _ in range(3):
             call()
         torch.cuda.synchronize()
@@ -349,8 +355,9 @@ def measure_gemm_modes(moe, layer, modes, call, main, dev, rounds=200):
         st, _ = layer.handle.stage_times()
         layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
         stages[f"mode{m}"] = {k: round(v, 5) for k, v in st.items()}
-    layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, 0)
-    return {"method": f"graph replays, {rounds} interleaved rounds; stages from 30 eager calls",
+    layer.handle.set_option(opt, restore)
+    return {"option": opt,
+            "method": f"graph replays, {rounds} interleaved rounds; stages from 30 eager calls",
             "ms": {n: _spread(v) for n, v in times.items()}, "stage_ms": stages}
 
 
@@ -518,6 +525,11 @@ def run_ours(args):
     if args.ab_gemm_modes:
         gemm_ab = measure_gemm_modes(moe, layer, [int(v) for v in args.ab_gemm_modes.split(",")], call, main, dev)
         layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, args.gemm_mode)
+    option_ab = None
+    if args.ab_option:
+        name, vals = args.ab_option.split("=")
+        option_ab = measure_gemm_modes(moe, layer, [int(v) for v in vals.split(",")], call, main, dev,
+                                       option=int(name), restore=int(vals.split(",")[-1]))
 
     peaks, peak_src = load_peaks()
     g1_ms = stage_ms["gemm_gate_up"]
@@ -601,6 +613,8 @@ def run_ours(args):
     }
     if gemm_ab is not None:
         result["gemm_mode_ab"] = gemm_ab
+    if option_ab is not None:
+        result["option_ab"] = option_ab
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
 

@@ -135,7 +135,13 @@ typedef enum {
    * kernels fill the SMs that routing and permutation leave idle (no fixed
    * split measured faster on the decode, MX, skewed or prefill workloads).
    * k > 0 = k SMs (at most half). The result is the same either way. */
-  MOE_OPT_SHARED_SMS = 4
+  MOE_OPT_SHARED_SMS = 4,
+  /* 1 (default) = in bf16 layers whose routed GEMM-1 takes the tokens-as-M
+   * tiling (more than 48 rows per expert on average, or mode 2), the GEMM-1
+   * loads its A rows straight from x through perm_src (InitRouting's row
+   * gather fused into the grouped GEMM) and x_perm is not written; 0 = the
+   * permutation writes x_perm and GEMM-1 reads it. The result is the same. */
+  MOE_OPT_GATHER_A = 5
 } moe_option_t;
 
 /* Stage indices reported by moe_read_stage_times. */

@@ -24,7 +24,8 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = range(6)
 MOE_BF16, MOE_MXFP8_E4M3, MOE_MXFP4_W4A8 = 0, 1, 2
 DTYPES = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8_E4M3, "mxfp4": MOE_MXFP4_W4A8}
-MOE_OPT_GEMM_MODE, MOE_OPT_STAGE_TIMING, MOE_OPT_WAIT_LIMIT_US, MOE_OPT_SHARED_FOLD, MOE_OPT_SHARED_SMS = 0, 1, 2, 3, 4
+(MOE_OPT_GEMM_MODE, MOE_OPT_STAGE_TIMING, MOE_OPT_WAIT_LIMIT_US, MOE_OPT_SHARED_FOLD, MOE_OPT_SHARED_SMS,
+ MOE_OPT_GATHER_A) = 0, 1, 2, 3, 4, 5
 STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine", "shared", "total"]
 DEV_TIMEOUT_SELFTEST = 4
 

@@ -38,6 +38,7 @@ struct moe_handle {
   int stage_timing = 0;
   int shared_fold = 0;  // MOE_OPT_SHARED_FOLD
   int shared_sms = 0;   // MOE_OPT_SHARED_SMS: 0 no split, k > 0 fixed
+  int gather_a = 1;     // MOE_OPT_GATHER_A
   uint64_t wait_limit_ns = kDefaultWaitLimitNs;
   cudaEvent_t* tev = nullptr;  // [kTimingRing][kEventsPerCall], created on first use
   int t_calls = 0;             // calls recorded since the last read
@@ -172,6 +173,9 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
   g.shared_w_gate = nullptr;
   g.shared_w_up = nullptr;
   g.shared_w_down = nullptr;
+  g.gather_src = nullptr;
+  g.gather_k = 0;
+  g.gather_x = nullptr;
   g.G = G;
   g.offsets = offsets;
   g.rows = rows;
@@ -311,6 +315,9 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
     case MOE_OPT_SHARED_SMS:
       if (value < 0) return MOE_ERR_INVALID_ARG;
       h->shared_sms = value;
+      return MOE_OK;
+    case MOE_OPT_GATHER_A:
+      h->gather_a = value ? 1 : 0;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -622,21 +629,6 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   if (e == cudaSuccess)
     e = launch_permute_index(topk_idx, TK, E, at<void>(ws, L.perm_scratch), counts, offsets,
                              tile_offsets, perm_src, flat_to_perm, h->status, sm);
-  // MX: the E4M3 rows and their scale atoms in one pass; bf16: the rows.
-  if (e == cudaSuccess)
-    e = mx ? launch_scatter_rows_mx(static_cast<const uint8_t*>(x), xq_s, T, H, flat_to_perm,
-                                    topk_idx, offsets, tile_offsets, K, TK, E,
-                                    static_cast<uint8_t*>(x_perm), at<uint8_t>(ws, L.x_perm_s),
-                                    h->status, sm)
-           : launch_scatter_rows(x, T, H * 2, flat_to_perm, K, TK, x_perm, h->status, sm);
-  if (e == cudaSuccess && fold) {  // group E: x itself, after the routed rows
-    set_i32_kernel<<<1, 1, 0, sm>>>(offsets + E + 1, TK + T);
-    e = cudaGetLastError();
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(static_cast<uint8_t*>(x_perm) + (size_t)TK * H * 2, x, (size_t)T * H * 2,
-                          cudaMemcpyDeviceToDevice, sm);
-  }
-  mark(2, sm);
   GroupedGemmArgs g = gemm_args(h, fold ? E + 1 : E, offsets, fold ? TK + T : TK, H, I, x_perm,
                                 w->w_gate, w->w_up, w->w_down, hbuf, y_perm,
                                 mx ? w->s_gate : nullptr, mx ? w->s_down : nullptr);
@@ -651,6 +643,29 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
     g.a_scale = at<uint8_t>(ws, L.x_perm_s);
     g.h_scale = at<uint8_t>(ws, L.h_s);
   }
+  // bf16, tokens-as-M: GEMM-1 gathers its A rows from x itself (InitRouting's
+  // row gather fused into the grouped GMM's load), so x_perm is not written.
+  const bool gather = !mx && !fold && h->gather_a && gemm_pick_mode(g) == kModeTokensM;
+  if (gather) {
+    g.gather_src = perm_src;
+    g.gather_k = K;
+    g.gather_x = x;
+  }
+  // MX: the E4M3 rows and their scale atoms in one pass; bf16: the rows.
+  if (e == cudaSuccess && !gather)
+    e = mx ? launch_scatter_rows_mx(static_cast<const uint8_t*>(x), xq_s, T, H, flat_to_perm,
+                                    topk_idx, offsets, tile_offsets, K, TK, E,
+                                    static_cast<uint8_t*>(x_perm), at<uint8_t>(ws, L.x_perm_s),
+                                    h->status, sm)
+           : launch_scatter_rows(x, T, H * 2, flat_to_perm, K, TK, x_perm, h->status, sm);
+  if (e == cudaSuccess && fold) {  // group E: x itself, after the routed rows
+    set_i32_kernel<<<1, 1, 0, sm>>>(offsets + E + 1, TK + T);
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(x_perm) + (size_t)TK * H * 2, x, (size_t)T * H * 2,
+                          cudaMemcpyDeviceToDevice, sm);
+  }
+  mark(2, sm);
   if (e == cudaSuccess) e = mx ? launch_gemm_mx_gate_up(g, sm) : launch_gemm_gate_up(g, sm);
   mark(3, sm);
   if (e == cudaSuccess) e = mx ? launch_gemm_mx_down(g, sm) : launch_gemm_down(g, sm);

@@ -57,10 +57,13 @@ constexpr int kMaxGroups = 1024;
 constexpr int kTopSlots = 8;       // gating epilogue: top-k kept in registers up to this K
 constexpr int kMaxSmem = 232448;   // 227 KB dynamic shared memory per CTA
 
-template <bool SWAP, int MODE, int BN>
+constexpr int kGatherThreads = 128;  // A-row loaders of the gathered GEMM-1: one row each
+
+template <bool SWAP, int MODE, int BN, bool GATHER = false>
 struct Geo {
   static constexpr int kTileBytes = 128 * 128;                       // 128 rows x 128 B
-  static constexpr int THREADS = 192;
+  // Gathered GEMM-1: warps 6..9 load the A rows (cp.async) beside the roles below.
+  static constexpr int THREADS = GATHER ? 192 + kGatherThreads : 192;
   static constexpr int ACT_ROWS = SWAP ? BN : 128;                   // activation rows / tile
   static constexpr int ACT_BYTES = ACT_ROWS * 128;                   // one 64-wide K slice
   static constexpr int W_BYTES = 2 * kTileBytes;                     // two 128-row weight boxes
@@ -93,6 +96,7 @@ struct Geo {
   static_assert(SMEM <= kMaxSmem, "shared memory budget");
   static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(!SWAP || (BN % 32 == 0 && BN >= 32 && BN <= 128), "token tile");
+  static_assert(!GATHER || (!SWAP && MODE == 0), "the gather feeds the tokens-as-M GEMM-1");
 };
 
 // Epilogue of one tile: TMEM accumulator (columns tb..) -> h (bf16, SwiGLU),
@@ -303,15 +307,15 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const TileInfo& 
   }
 }
 
-template <bool SWAP, int MODE, int BN>
-__global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
+template <bool SWAP, int MODE, int BN, bool GATHER>
+__global__ void __launch_bounds__(Geo<SWAP, MODE, BN, GATHER>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_act,
                         const __grid_constant__ CUtensorMap map_w0,
                         const __grid_constant__ CUtensorMap map_w1,
                         const __grid_constant__ CUtensorMap map_y,
                         const __grid_constant__ CUtensorMap map_w0s,
                         const __grid_constant__ CUtensorMap map_w1s, const KParams p) {
-  using Gm = Geo<SWAP, MODE, BN>;
+  using Gm = Geo<SWAP, MODE, BN, GATHER>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
@@ -345,7 +349,9 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
   fill_row_start(p, row_start, threadIdx.x, Gm::THREADS);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(full_bar(s), 1);
+      // Gathered: the producer's arrive (weights by TMA) and one asynchronous
+      // arrive per loader thread once its copies of the stage have landed.
+      mbar_init(full_bar(s), GATHER ? 1 + kGatherThreads : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -423,9 +429,9 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
           }
           const int kx = kb * kBK;
           const uint32_t fb = full_bar(rg.s);
-          mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+          mbar_arrive_expect_tx(fb, GATHER ? Gm::W_BYTES : Gm::STAGE_BYTES);
           const uint32_t st = base_u32 + rg.s * Gm::STAGE_BYTES;
-          tma_load_2d(st + Gm::ACT_OFF, &map_act, fb, kx, act_row);
+          if (!GATHER) tma_load_2d(st + Gm::ACT_OFF, &map_act, fb, kx, act_row);
           if (SWAP) {
             tma_load_2d_hint(st + Gm::W_OFF, mw0, fb, kx, w_row0, pol_w);
             tma_load_2d_hint(st + Gm::W_OFF + Gm::kTileBytes, mw1, fb, kx, w_row1, pol_w);
@@ -465,6 +471,9 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
             ok = false;
             break;
           }
+          // Gathered A rows were written by cp.async (the generic proxy); the
+          // tensor cores read through the async proxy.
+          if (GATHER) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t st = base_u32 + rg.s * Gm::STAGE_BYTES;
           const uint32_t sA = st + (SWAP ? Gm::W_OFF : Gm::ACT_OFF);
@@ -490,6 +499,56 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN>::THREADS, 1)
         drain_wait(drain_bar, 0, 100000000ull);
       }
     }
+  } else if (GATHER && warp >= 6) {
+    // ------------------------------------------------------------ A loader
+    // Each loader warp fills 32 of the tile's 128 A rows, four rows per
+    // instruction: lane l copies 16-byte chunk c = l % 8 of row 4i + l / 8 of
+    // the warp's rows (one 128-byte line per row and stage, so a warp
+    // instruction reads four whole lines). A row holds token gather_src[row]
+    // / gather_k of x; chunk c lands at position c ^ (row % 8) of the row's
+    // 128 bytes (the 128-byte swizzle the MMA descriptors expect). Rows past
+    // the group's end are not loaded (their accumulator rows are never
+    // stored). Each thread arrives on the stage's full barrier when its
+    // copies have landed.
+    const int lw = warp - 6;            // loader warp 0..3
+    const int c = lane & 7, sub = lane >> 3;
+    const uint8_t* x = static_cast<const uint8_t*>(p.gather_x);
+    const size_t row_bytes = (size_t)p.num_kb * kBK * 2;
+    Ring rg;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile_s<Gm::ACT_ROWS>(p.G, tile_start, row_start, tile);
+      const uint8_t* src[8];
+      uint32_t off[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rho = lw * 32 + i * 4 + sub;  // row within the tile
+        const int r = ti.tt * Gm::ACT_ROWS + rho;
+        src[i] = nullptr;
+        if (r < ti.nrows) {
+          const int f = __ldg(p.gather_src + ti.row0 + r);
+          if ((unsigned)f < (unsigned)p.rows) src[i] = x + (size_t)(f / p.gather_k) * row_bytes + c * 16;
+        }
+        off[i] = (uint32_t)(rho * 128 + ((c ^ (rho & 7)) << 4));
+      }
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        int go = 1;
+        if (lane == 0)
+          go = mbar_wait_bounded(empty_bar(rg.s), rg.ph ^ 1u, abort_flag, p.status,
+                                 MOE_DEV_TIMEOUT_PRODUCER, p.limit_ns) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = base_u32 + rg.s * Gm::STAGE_BYTES + Gm::ACT_OFF;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (src[i]) cp_async_16(dst + off[i], src[i] + (size_t)kb * 128);
+        cp_async_arrive_noinc(full_bar(rg.s));
+        rg.next(NS);
+      }
+    }
+    cp_async_wait_all();  // this thread's copies have landed before the CTA tears down
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
@@ -605,9 +664,9 @@ bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t ou
 
 namespace {
 
-template <bool SWAP, int MODE, int BN>
+template <bool SWAP, int MODE, int BN, bool GATHER = false>
 cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
-  using Gm = Geo<SWAP, MODE, BN>;
+  using Gm = Geo<SWAP, MODE, BN, GATHER>;
   const int Kdim = MODE == 0 ? a.H : a.I;
   const int N = MODE == 0 ? a.I : a.H;
   const void* act = MODE == 0 ? a.a : a.h;
@@ -619,10 +678,11 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const bool fold = a.shared_w_gate != nullptr && a.offsets != nullptr;
   const int Gw = fold ? G - 1 : G;  // groups whose weights are in w0 / w1
   CUtensorMap m_act, m_w0, m_w1, m_y, m_w0s, m_w1s;
-  if (!make_map(&m_act, act, false, Kdim, a.rows, Gm::ACT_ROWS) ||
+  if ((!GATHER && !make_map(&m_act, act, false, Kdim, a.rows, Gm::ACT_ROWS)) ||
       !make_map(&m_w0, w0, false, Kdim, (uint64_t)Gw * N, 128) ||
       !make_map(&m_w1, w1, false, Kdim, (uint64_t)Gw * N, 128))
     return cudaErrorInvalidValue;
+  if (GATHER) m_act = m_w0;  // unused: the A rows are gathered
   if (fold) {
     const void* s0 = MODE == 0 ? a.shared_w_gate : a.shared_w_down;
     const void* s1 = MODE == 0 ? a.shared_w_up : a.shared_w_down;
@@ -633,7 +693,7 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     m_w0s = m_w0;  // unused
     m_w1s = m_w1;
   }
-  auto kern = grouped_gemm_kernel<SWAP, MODE, BN>;
+  auto kern = grouped_gemm_kernel<SWAP, MODE, BN, GATHER>;
   KParams p = {};
   p.offsets = a.offsets;
   p.G = G;
@@ -649,6 +709,9 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   p.scaling = a.scaling;
   p.route_norm = a.route_norm;
   p.fold_group = fold ? G - 1 : -1;
+  p.gather_src = GATHER ? a.gather_src : nullptr;
+  p.gather_k = a.gather_k;
+  p.gather_x = a.gather_x;
   const long long n_wt = (N + Gm::W_COLS - 1) / Gm::W_COLS;
   const long long max_tiles = n_wt * ((a.rows + Gm::ACT_ROWS - 1) / Gm::ACT_ROWS + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
@@ -662,10 +725,11 @@ cudaError_t run_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <bool SWAP, int MODE, int BN>
+template <bool SWAP, int MODE, int BN, bool GATHER = false>
 cudaError_t set_smem_attribute() {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<SWAP, MODE, BN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<SWAP, MODE, BN>::SMEM);
+  return cudaFuncSetAttribute(grouped_gemm_kernel<SWAP, MODE, BN, GATHER>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Geo<SWAP, MODE, BN, GATHER>::SMEM);
 }
 
 int pick_mode(const GroupedGemmArgs& a) {
@@ -687,6 +751,7 @@ cudaError_t launch_mode(const GroupedGemmArgs& a, cudaStream_t s) {
     case kModePair:
       return MODE == 0 ? launch_gemm_pair_gate_up(a, s) : launch_gemm_pair_down(a, s);
     default:
+      if (MODE == 0 && a.gather_src) return run_gemm<false, 0, 32, true>(a, s);
       return run_gemm<false, MODE, 32>(a, s);
   }
 }
@@ -709,11 +774,14 @@ cudaError_t gemm_prepare_device() {
   const cudaError_t errs[] = {
       set_smem_attribute<true, 0, 32>(), set_smem_attribute<false, 0, 32>(),
       set_smem_attribute<true, 1, 32>(), set_smem_attribute<false, 1, 32>(),
-      set_smem_attribute<false, 2, 32>(), gemm_pair_prepare_device()};
+      set_smem_attribute<false, 2, 32>(), set_smem_attribute<false, 0, 32, true>(),
+      gemm_pair_prepare_device()};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
 }
+
+int gemm_pick_mode(const GroupedGemmArgs& a) { return pick_mode(a); }
 
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
   return launch_mode<0>(a, s);

@@ -27,6 +27,11 @@ struct KParams {
   uint8_t* out_scale;
   // Group that takes the second weight maps (a folded shared expert), or -1.
   int fold_group;
+  // GEMM-1 with the row gather in its A load: row r of group g is token
+  // gather_src[r] / gather_k of gather_x ([T, H] bf16); nullptr: a is given.
+  const int32_t* gather_src;
+  int gather_k;
+  const void* gather_x;
   // Gating (MODE 2): routing outputs [rows, topk]; `out` (nullable) takes the logits.
   int32_t* topk_idx;
   float* topk_w;

@@ -93,6 +93,12 @@ struct GroupedGemmArgs {
   const uint8_t* s_gate;
   const uint8_t* s_down;
   int w4;
+  // bf16 GEMM-1, tokens-as-M tiling: gather the A rows from x instead of
+  // reading a: row r is token gather_src[r] / gather_k of gather_x [T, H]
+  // (nullptr: read a).
+  const int32_t* gather_src;
+  int gather_k;
+  const void* gather_x;
   // bf16 only: the shared expert's [I, H], [I, H], [H, I] weights, run as the
   // last of the G groups (nullptr: every group uses w_gate / w_up / w_down).
   const void* shared_w_gate;
@@ -124,6 +130,8 @@ bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t ou
 cudaError_t gemm_mx_prepare_device();
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s);
+// The tiling launch_gemm_gate_up / launch_gemm_down will use (GemmMode).
+int gemm_pick_mode(const GroupedGemmArgs& a);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_down(const GroupedGemmArgs& a, cudaStream_t s);
 // CTA-pair bf16 grouped GEMM (gemm_pair.cu); not for a folded shared expert.

@@ -111,6 +111,19 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the arrive on an
+// mbarrier once every cp.async this thread issued so far has landed (counted
+// as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // 2-D tiled bulk tensor store shared -> global (bulk-group completion). The
 // source holds the box in the tensor map's swizzled layout.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
