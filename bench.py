@@ -35,15 +35,20 @@ METRIC = ("MoE-layer tokens/sec at Hy3 shape; achieved HBM GB/s (decode) and TFL
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the routed
-# GEMM-1 launch in one ncu capture of each full workload at seed 0 (summarised
-# in profiles/gemm1_traffic_full_size.md). A value is reported only while the
-# kernel source still hashes as it did for the capture, and only for the
-# workload as captured (no --experts override).
-GEMM1_TRAFFIC = {
-    "decode": ("gemm.cu", "7af4e1ec06e05eed", 4559366400 + 3940864),
-    "prefill": ("gemm.cu", "7af4e1ec06e05eed", 5519865344 + 197731840),
-    "mxfp8": ("gemm_mx.cu", "02a99fab6e6d588b", 2565780736 + 27886592),
-    "mxfp4": ("gemm_mx.cu", "02a99fab6e6d588b", 1354861056 + 26868992),
+# GEMM-1 launch, captured with ncu on a reduced-expert case of each workload
+# (decode, MXFP8 and W4A8 at E = 48, prefill at E = 32; summarised in
+# profiles/gemm1_traffic_reduced_e.md), as a ratio to that case's algorithmic
+# GEMM-1 bytes. The full workload's traffic is reported as that ratio times
+# its own algorithmic bytes (traffic grows with the bytes the launch must
+# move: the touched experts' weights, the activation rows, h). A value is
+# reported only while the GEMM sources still hash as they did for the capture.
+GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_sched.cuh", "ptx.cuh")
+GEMM1_TRAFFIC_SHA = "125e3a614070d27e"
+GEMM1_TRAFFIC_RATIO = {
+    "decode": (1212221696 + 2967552) / 1213726720,   # E = 48
+    "prefill": (1169254144 + 191149824) / 1073741824,  # E = 32, A rows gathered from x
+    "mxfp8": (692713728 + 24632320) / 718012416,     # E = 48
+    "mxfp4": (390618880 + 22769920) / 416022528,     # E = 48
 }
 
 
@@ -63,6 +68,8 @@ def parse():
     ap.add_argument("--shared-fold", action="store_true",
                     help="run the shared expert as one more group of the routed GEMMs (bf16, I_shared == I)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="skip the shared-expert overlap measurement (shorter runs, e.g. under a profiler)")
     ap.add_argument("--gemm-mode", type=int, default=0,
                     help="MOE_OPT_GEMM_MODE for the timed calls (0 automatic, 1 weights-as-M, 2 tokens-as-M, 3 CTA pair)")
     ap.add_argument("--ab-gemm-modes", default="",
@@ -185,8 +192,10 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def algorithmic_work(shape, counts, gated=False):
-    """Bytes the layer must move and FLOPs it must do, from the expert counts."""
+def algorithmic_work(shape, counts, gated=False, gathered=False):
+    """Bytes the layer must move and FLOPs it must do, from the expert counts.
+    gathered: GEMM-1 reads its A rows from x itself (T rows) instead of from
+    the permuted copy (T*K rows)."""
     H, I, Is, T, E, K = shape.H, shape.I, shape.I_shared, shape.T, shape.E, shape.K
     touched = int((counts > 0).sum())
     # Bytes per GEMM operand element: bf16, or an MX code (E4M3: 1 byte, E2M1:
@@ -202,8 +211,9 @@ def algorithmic_work(shape, counts, gated=False):
     layer_bytes = int(touched * w_expert + w_shared + T * H * 2 + (E * H * 2 if gated else T * E * 4) + T * H * 2)
     flops = 6 * H * I * T * K + 6 * H * Is * T + (2 * T * H * E if gated else 0)
     TK = T * K
-    # GEMM-1 reads the touched experts' gate/up weights and x_perm, and writes h.
-    gemm1_bytes = int(touched * 2 * I * H * wb + TK * H * ab + TK * I * ab)
+    # GEMM-1 reads the touched experts' gate/up weights and x_perm (or, gathered,
+    # x), and writes h.
+    gemm1_bytes = int(touched * 2 * I * H * wb + (T if gathered else TK) * H * ab + TK * I * ab)
     return dict(touched=touched, layer_bytes=layer_bytes, flops=flops, gemm1_bytes=gemm1_bytes,
                 gemm1_flops=4 * H * I * TK)
 
@@ -254,10 +264,12 @@ def cpu_oracle_rate(shape, x, logits, w, budget_s: float, max_tokens: int | None
     return n / dt, n, dt, oracle.num_threads()
 
 
-def source_sha(name):
-    p = os.path.join(ROOT, "routed_expert_ffn_04_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "routed_expert_ffn_04_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def time_graph(call, args, main, dev, world):
@@ -444,7 +456,11 @@ def run_ours(args):
     else:
         moe.route(layer.handle, cfg, logits, idx, tw)
     counts = torch.bincount(idx.flatten().long(), minlength=shape.E).cpu().numpy()
-    work = algorithmic_work(shape, counts, gated=args.gated)
+    # The layer's default path: bf16 GEMM-1 takes the tokens-as-M tiling above
+    # 48 rows per expert on average, and then gathers its A rows from x.
+    gathered = (shape.dtype == "bf16" and not args.shared_fold and args.gemm_mode in (0, 2)
+                and (args.gemm_mode == 2 or shape.T * shape.K > 48 * shape.E))
+    work = algorithmic_work(shape, counts, gated=args.gated, gathered=gathered)
 
     def call():
         if args.gated:
@@ -518,7 +534,7 @@ def run_ours(args):
     # the main stream, and the layer without a shared expert. The shared MLP
     # alone costs serial - none; the second stream hides (serial - two) of it.
     overlap = None
-    if shape.I_shared and not (args.shared_fold and shape.dtype == "bf16"):
+    if shape.I_shared and not args.no_overlap and not (args.shared_fold and shape.dtype == "bf16"):
         overlap = measure_overlap(moe, layer, shape, cfg, x, logits, w_router, out, main, dev, args)
 
     gemm_ab = None
@@ -543,10 +559,9 @@ def run_ours(args):
         peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         unit = "TFLOP/s"
     traffic = None
-    if args.workload in GEMM1_TRAFFIC and not args.experts:
-        src, sha, nbytes = GEMM1_TRAFFIC[args.workload]
-        if source_sha(src) == sha:
-            traffic = nbytes
+    if (args.workload in GEMM1_TRAFFIC_RATIO and not args.experts and not args.gated and not args.shared_fold
+            and args.gemm_mode == 0 and source_sha(GEMM1_TRAFFIC_SOURCES) == GEMM1_TRAFFIC_SHA):
+        traffic = int(round(GEMM1_TRAFFIC_RATIO[args.workload] * work["gemm1_bytes"]))
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     # route 1; permute 1 (one block up to 16384 pairs, else 3) + row gather 1;
