@@ -95,10 +95,12 @@ typedef struct {
  *   s_down  = atoms of down (moe_pack_mx_scales(down, NULL)),
  *   s_up    unused (NULL); ss_gate, ss_up, ss_down the same for the shared
  *   expert. Every scale pointer 16-byte aligned.
- * MXFP4_W4A8 mode: as MXFP8, except that the routed w_gate, w_up [E, I, H/2]
- *   and w_down [E, H, I/2] hold packed E2M1 codes (two per byte, element 2j
- *   in the low nibble; moe_quantize_mxfp4), 32-byte aligned. Their scales and
- *   the shared expert (E4M3 + atoms) are as in MXFP8 mode. */
+ * MXFP4_W4A8 mode: as MXFP8, except that the routed weights are packed E2M1
+ *   codes (two per byte, element 2j in the low nibble; moe_quantize_mxfp4) in
+ *   tile order: w_gate = moe_tile_mxfp4_weights(gate, up) of the [E*I, H]
+ *   gate and up codes together, w_up unused (NULL), w_down =
+ *   moe_tile_mxfp4_weights(down, NULL) of [E*H, I]; 32-byte aligned. Their
+ *   scales and the shared expert (E4M3 + atoms) are as in MXFP8 mode. */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
   const uint8_t *s_gate, *s_up, *s_down;
@@ -141,7 +143,12 @@ typedef enum {
    * loads its A rows straight from x through perm_src (InitRouting's row
    * gather fused into the grouped GEMM) and x_perm is not written; 0 = the
    * permutation writes x_perm and GEMM-1 reads it. The result is the same. */
-  MOE_OPT_GATHER_A = 5
+  MOE_OPT_GATHER_A = 5,
+  /* Weight rows per MMA of the MX (MXFP8, W4A8) grouped GEMM-1: 0 = automatic
+   * (default: 256 for E2M1 weights, 128 for E4M3), 1 = 128 (gate 64 + up 64,
+   * double-buffered accumulators), 2 = 256 (gate 128 + up 128, one
+   * accumulator). The result is the same up to fp32 summation order. */
+  MOE_OPT_MX_TILE = 6
 } moe_option_t;
 
 /* Stage indices reported by moe_read_stage_times. */
@@ -219,8 +226,10 @@ MOE_API moe_status_t moe_grouped_gemm_workspace_size(int rows, int num_groups, i
  *   GEMM-2, as the W8A8 path quantises every Linear input ([Hy3] section
  *   8.2). Operands and scales go to the block-scaled tensor cores as stored.
  *   H % 128 == 0, I % 128 == 0.
- * MXFP4_W4A8: w_* hold packed E2M1 codes ([num_groups, I, H/2] and
- *   [num_groups, H, I/2], 32-byte aligned); scales and a as in MXFP8.
+ * MXFP4_W4A8: w_gate = moe_tile_mxfp4_weights(gate, up) of the packed E2M1
+ *   codes of [num_groups*I, H] gate and up weights, w_up unused, w_down =
+ *   moe_tile_mxfp4_weights(down, NULL) of [num_groups*H, I]; 32-byte aligned;
+ *   scales and a as in MXFP8.
  * offsets (device): [num_groups + 1] int32, non-decreasing, offsets[0] = 0,
  *   offsets[num_groups] <= rows; NULL means one group of all rows (a dense
  *   SwiGLU MLP, used for the shared expert).
@@ -268,6 +277,26 @@ MOE_API moe_status_t moe_quantize_mxfp8(moe_handle_t h, const void* in_bf16, int
  * cols/32] uint8 out. cols % 32 == 0. */
 MOE_API moe_status_t moe_quantize_mxfp4(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream);
+
+/* Tile order of packed E2M1 weights, the form the W4A8 grouped GEMMs read
+ * (a one-time weight step, like the page's weight conversion, section 五
+ * "转换权重", which derives the MXFP4 routed-expert weights for the MoE GMM).
+ * q0, q1 (device): [rows, cols/2] packed E2M1 as moe_quantize_mxfp4 writes it.
+ * tiled (device): one contiguous block per 128-row block t and 128-element K
+ * block kb (K blocks of a row block consecutive, row blocks in order), the
+ * rows of 64 bytes each:
+ *   q1 == NULL (w_down): 8 KB at byte 8192 (t * (cols/128) + kb), rows
+ *     128 t .. 128 t + 127 of q0; tiled holds rows * cols/2 bytes.
+ *   q1 != NULL (w_gate = q0, w_up = q1, packed together as
+ *     moe_pack_mx_scales packs their scales): 16 KB at byte 16384 (t *
+ *     (cols/128) + kb): rows 0-63 of the block from q0, then from q1, then
+ *     rows 64-127 from q0, then from q1; tiled holds 2 * rows * cols/2 bytes.
+ * One such block is exactly what one TMA load of the W4A8 GEMM-1 (a pair
+ * block) or GEMM-2 (a w_down block) fetches per K stage, so a stage is one
+ * contiguous read and one copy instruction. rows % 128 == 0, cols % 128 == 0,
+ * tiled distinct from q0 and q1, all 16-byte aligned. */
+MOE_API moe_status_t moe_tile_mxfp4_weights(moe_handle_t h, const uint8_t* q0, const uint8_t* q1, int64_t rows,
+                                            int cols, uint8_t* tiled, moe_stream_t stream);
 
 /* Scale atoms for the block-scaled MXFP8 GEMM from row-major E8M0 scales
  * (as moe_quantize_mxfp8 writes them). An atom holds the scales of 128 rows

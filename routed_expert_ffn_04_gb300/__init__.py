@@ -25,7 +25,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
 MOE_BF16, MOE_MXFP8_E4M3, MOE_MXFP4_W4A8 = 0, 1, 2
 DTYPES = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8_E4M3, "mxfp4": MOE_MXFP4_W4A8}
 (MOE_OPT_GEMM_MODE, MOE_OPT_STAGE_TIMING, MOE_OPT_WAIT_LIMIT_US, MOE_OPT_SHARED_FOLD, MOE_OPT_SHARED_SMS,
- MOE_OPT_GATHER_A) = 0, 1, 2, 3, 4, 5
+ MOE_OPT_GATHER_A, MOE_OPT_MX_TILE) = 0, 1, 2, 3, 4, 5, 6
 STAGES = ["route", "permute", "gemm_gate_up", "gemm_down", "combine", "shared", "total"]
 DEV_TIMEOUT_SELFTEST = 4
 
@@ -82,6 +82,7 @@ def load(build_if_missing: bool = False):
         "moe_combine": [P, P, P, P, P, P, P, P],
         "moe_quantize_mxfp8": [P, P, ctypes.c_int64, I, P, P, P],
         "moe_quantize_mxfp4": [P, P, ctypes.c_int64, I, P, P, P],
+        "moe_tile_mxfp4_weights": [P, P, P, ctypes.c_int64, I, P, P],
         "moe_pack_mx_scales": [P, P, P, ctypes.c_int64, I, P, P],
         "moe_layer_forward": [P, P, P, P, P, P, P, P, S, P, P],
         "moe_layer_forward_host": [P, P, P, P, P, P, P, S, P, P],
@@ -279,11 +280,29 @@ def pack_mx_scales(h: Handle, scale0, scale1=None, stream=None):
     return out
 
 
+def tile_mxfp4(h: Handle, q0, q1=None, stream=None):
+    """Tile order (moe_tile_mxfp4_weights) of packed E2M1 codes [..., rows, cols/2]:
+    of q0 alone (same shape), or of the gate (q0) / up (q1) pair (twice the
+    rows)."""
+    rows = q0.numel() // q0.shape[-1]
+    shape = q0.shape if q1 is None else q0.shape[:-2] + (2 * q0.shape[-2], q0.shape[-1])
+    out = torch.empty(shape, dtype=torch.uint8, device=q0.device)
+    _check(load().moe_tile_mxfp4_weights(h.ptr, _p(q0), _p(q1), int(rows), int(q0.shape[-1] * 2), _p(out),
+                                         _stream(stream)), "moe_tile_mxfp4_weights")
+    return out
+
+
 def pack_weights_mx(h: Handle, mx: dict, stream=None) -> dict:
     """Codes + row-major scales (quantize_weights_mx) -> the weight form the
-    MXFP8 layer takes: s_gate / ss_gate = gate+up atoms, s_down / ss_down =
-    down atoms, s_up / ss_up dropped."""
+    MX layer takes: s_gate / ss_gate = gate+up atoms, s_down / ss_down =
+    down atoms, s_up / ss_up dropped; packed E2M1 routed codes (W4A8) in tile
+    order: w_gate = the gate/up pair, w_up dropped, w_down alone."""
     out = {k: v for k, v in mx.items() if not k.startswith("s")}
+    wg, sg = mx.get("w_gate"), mx.get("s_gate")
+    if wg is not None and sg is not None and wg.shape[-1] * 2 == sg.shape[-1] * 32:  # packed E2M1
+        out["w_gate"] = tile_mxfp4(h, wg, mx["w_up"], stream=stream)
+        out["w_up"] = None
+        out["w_down"] = tile_mxfp4(h, mx["w_down"], stream=stream)
     for p in ("s_", "ss_"):
         if mx.get(p + "gate") is None:
             continue

@@ -39,6 +39,7 @@ struct moe_handle {
   int shared_fold = 0;  // MOE_OPT_SHARED_FOLD
   int shared_sms = 0;   // MOE_OPT_SHARED_SMS: 0 no split, k > 0 fixed
   int gather_a = 1;     // MOE_OPT_GATHER_A
+  int mx_tile = 0;      // MOE_OPT_MX_TILE
   uint64_t wait_limit_ns = kDefaultWaitLimitNs;
   cudaEvent_t* tev = nullptr;  // [kTimingRing][kEventsPerCall], created on first use
   int t_calls = 0;             // calls recorded since the last read
@@ -170,6 +171,7 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
   g.s_gate = sg;
   g.s_down = sd;
   g.w4 = 0;
+  g.mx_tile = 0;
   g.shared_w_gate = nullptr;
   g.shared_w_up = nullptr;
   g.shared_w_down = nullptr;
@@ -188,6 +190,7 @@ GroupedGemmArgs gemm_args(moe_handle_t h, int G, const int32_t* offsets, int row
   g.h = hbuf;
   g.y = y;
   g.mode = h->gemm_mode;
+  g.mx_tile = h->mx_tile;
   g.num_sms = h->num_sms;
   g.status = h->status;
   g.wait_limit_ns = h->wait_limit_ns;
@@ -319,6 +322,10 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
     case MOE_OPT_GATHER_A:
       h->gather_a = value ? 1 : 0;
       return MOE_OK;
+    case MOE_OPT_MX_TILE:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      h->mx_tile = value;
+      return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -418,7 +425,8 @@ MOE_API moe_status_t moe_grouped_swiglu_gemm(moe_handle_t h, int num_groups, int
   if (dtype != MOE_BF16 && !is_mx(dtype)) return MOE_ERR_INVALID_ARG;
   const bool mx = is_mx(dtype);
   const bool w4 = dtype == MOE_MXFP4_W4A8;
-  if (!a || !w_gate || !w_up || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
+  // W4A8: w_gate holds the gate and up codes together, w_up is unused.
+  if (!a || !w_gate || (!w_up && !w4) || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
   if (mx && (!a_scale || !s_gate || !s_down || H % 128 || I % 128)) return MOE_ERR_INVALID_ARG;
   if (w4 && !weights_aligned32(w_gate, w_up, w_down)) return MOE_ERR_INVALID_ARG;
   (void)s_up;  // MXFP8: s_gate holds the gate and up scale atoms together
@@ -476,6 +484,16 @@ MOE_API moe_status_t moe_pack_mx_scales(moe_handle_t h, const uint8_t* scale0,
       launch_pack_weight_scales(scale0, scale1, rows, cols, atoms, static_cast<cudaStream_t>(stream)));
 }
 
+MOE_API moe_status_t moe_tile_mxfp4_weights(moe_handle_t h, const uint8_t* q0, const uint8_t* q1, int64_t rows,
+                                            int cols, uint8_t* tiled, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 || rows % 128) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!q0 || !tiled || q0 == tiled || q1 == tiled)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(q0) || !aligned16(q1) || !aligned16(tiled)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_handle(h);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_tile_e2m1(q0, q1, rows, cols, tiled, static_cast<cudaStream_t>(stream)));
+}
+
 MOE_API moe_status_t moe_quantize_mxfp4(moe_handle_t h, const void* in_bf16, int64_t rows,
                                         int cols, uint8_t* q, uint8_t* scale, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 32) return MOE_ERR_INVALID_ARG;
@@ -509,10 +527,11 @@ static moe_status_t layer_forward_impl(moe_handle_t h, const moe_config_t* cfg,
   const bool has_shared = cfg->I_shared > 0;
   if (cfg->T > 0 && (!x || (!logits && !w_router) || !out)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_router)) return MOE_ERR_INVALID_ARG;
-  if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
-  if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
   const bool mx = is_mx(cfg->dtype);
   const bool w4 = cfg->dtype == MOE_MXFP4_W4A8;  // routed experts E2M1; shared stays E4M3
+  // W4A8: w_gate holds the routed gate and up codes together, w_up is unused.
+  if (!w->w_gate || (!w->w_up && !w4) || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (has_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOE_ERR_INVALID_ARG;
   // Pre-quantised activations: only in MX mode, and only with given logits
   // (the router reads bf16 x).
   if (x_scale && (!mx || w_router)) return MOE_ERR_INVALID_ARG;

@@ -649,10 +649,10 @@ bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
   return make_map(m, ptr, true, inner, outer, box_rows);
 }
 
-bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
-  if (!g_encode || inner % 128 || (reinterpret_cast<uintptr_t>(ptr) & 31)) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner / 2};
+bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t rows64, uint32_t box_rows) {
+  if (!g_encode || box_rows == 0 || box_rows > 256 || (reinterpret_cast<uintptr_t>(ptr) & 31)) return false;
+  const cuuint64_t dims[2] = {128, rows64};
+  const cuuint64_t strides[1] = {64};
   const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims,

@@ -10,10 +10,12 @@
 //   GEMM-2 (MODE 1): y = h Wd^T, fp32
 //
 // W4 (the W4A8 recipe of the same section: MXFP4 routed-expert weights, MXFP8
-// activations): the weights are packed E2M1, TMA-loaded through a 16U4 tensor
-// map that puts each 16 codes in the low half of a 16-byte slot, the operand
-// layout kind::mxf8f6f4 reads for E2M1 (B format code 5). Shared-memory tiles,
-// scales and the MMA shape are those of E4M3; HBM weight bytes halve.
+// activations): the weights are packed E2M1 in tile order
+// (moe_tile_mxfp4_weights: a stage's 128 weight rows are one contiguous block,
+// one TMA load), loaded through a 16U4 tensor map that puts each 16 codes in
+// the low half of a 16-byte slot, the operand layout kind::mxf8f6f4 reads for
+// E2M1 (B format code 5). Shared-memory tiles, scales and the MMA shape are
+// those of E4M3; HBM weight bytes halve.
 //
 // Scales travel in scale atoms (mx_layout.cuh): 512 bytes per 128 rows x 128
 // K elements, already in the order the block-scaled MMA reads from TMEM.
@@ -199,8 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf = sf_smem0 + rg.s * kSfBytes;
           const int kx = kb * kK;
           tma_load_2d(st, &map_act, fb, kx, act_row);
-          tma_load_2d_hint(st + kTileBytes, &map_w0, fb, kx, w_row0, pol);
-          tma_load_2d_hint(st + kTileBytes + kTileBytes / 2, &map_w1, fb, kx, w_row1, pol);
+          if (W4) {
+            // Tile order: the tile's 128 weight rows (GEMM-1: gate 64 + up 64,
+            // half wt & 1 of a 256-row pair block) are one contiguous block.
+            const int t = MODE == 0 ? ti.g * (p.N / 128) + ti.wt / 2 : ti.g * (p.N / 128) + ti.wt;
+            const int y = MODE == 0 ? (t * n_k + kb) * 256 + (ti.wt & 1) * 128 : (t * n_k + kb) * 128;
+            tma_load_2d_hint(st + kTileBytes, &map_w0, fb, 0, y, pol);
+          } else {
+            tma_load_2d_hint(st + kTileBytes, &map_w0, fb, kx, w_row0, pol);
+            tma_load_2d_hint(st + kTileBytes + kTileBytes / 2, &map_w1, fb, kx, w_row1, pol);
+          }
           bulk_load_hint(sf, a_atoms + (size_t)kb * kAtomBytes, kAtomBytes, fb, pol);
           bulk_load_hint(sf + kAtomBytes, b_atoms + (size_t)kb * kAtomBytes, kAtomBytes, fb, pol);
           armed.mark(rg);
@@ -414,10 +424,15 @@ cudaError_t run_gemm_mx(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.H % 128 || a.I % 128 || a.G > kMaxGroups) return cudaErrorInvalidValue;
   const int G = a.offsets ? a.G : 1;
   CUtensorMap m_act, m_w0, m_w1, m_y;
-  auto wmap = W4 ? make_tmap_e2m1 : make_tmap_u8;
-  if (!make_tmap_u8(&m_act, act, Kdim, a.rows, 128) || !wmap(&m_w0, w0, Kdim, (uint64_t)G * N, 64) ||
-      !wmap(&m_w1, w1, Kdim, (uint64_t)G * N, 64))
-    return cudaErrorInvalidValue;
+  bool maps_ok = make_tmap_u8(&m_act, act, Kdim, a.rows, 128);
+  if (W4) {  // tile order (moe_tile_mxfp4_weights): GEMM-1 a gate/up pair, GEMM-2 one matrix
+    maps_ok = maps_ok && make_tmap_e2m1(&m_w0, w0, (MODE == 0 ? 2ull : 1ull) * G * N * (Kdim / 128), 128);
+    m_w1 = m_w0;
+  } else {
+    maps_ok = maps_ok && make_tmap_u8(&m_w0, w0, Kdim, (uint64_t)G * N, 64) &&
+              make_tmap_u8(&m_w1, w1, Kdim, (uint64_t)G * N, 64);
+  }
+  if (!maps_ok) return cudaErrorInvalidValue;
   KParams p = {};
   p.offsets = a.offsets;
   p.G = G;
@@ -453,10 +468,14 @@ cudaError_t gemm_mx_prepare_device() {
       cudaFuncSetAttribute(grouped_gemm_mx_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
-  return cudaSuccess;
+  return gemm_mx_wide_prepare_device();
 }
 
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
+  // Automatic: the 256-row tile for E2M1 weights, whose 128-row GEMM-1 is
+  // bound by its MMA issue rate; E4M3 weights stream at the HBM rate either way.
+  if ((a.mx_tile == 2 || (a.mx_tile == 0 && a.w4)) && gemm_mx_wide_supported(a))
+    return launch_gemm_mx_wide_gate_up(a, s);
   return a.w4 ? run_gemm_mx<0, true>(a, s) : run_gemm_mx<0, false>(a, s);
 }
 

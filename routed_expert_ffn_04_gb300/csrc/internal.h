@@ -93,6 +93,9 @@ struct GroupedGemmArgs {
   const uint8_t* s_gate;
   const uint8_t* s_down;
   int w4;
+  // MX GEMM-1 weight tile: 0 auto, 1 = 128 rows (gemm_mx.cu), 2 = 256 rows
+  // (gemm_mx_wide.cu).
+  int mx_tile;
   // bf16 GEMM-1, tokens-as-M tiling: gather the A rows from x instead of
   // reading a: row r is token gather_src[r] / gather_k of gather_x [T, H]
   // (nullptr: read a).
@@ -119,17 +122,23 @@ bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t out
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
 // 2-D uint8 tensor map [outer, inner], box {128 bytes, box_rows}, 128-byte swizzle.
 bool make_tmap_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
-// 2-D packed E2M1 tensor map [outer, inner elements] (inner / 2 bytes per row;
-// inner % 128 == 0, ptr 32-byte aligned), box {128 elements, box_rows}: each
-// 16 codes (8 bytes) land in the low half of a 16-byte shared-memory slot,
-// 128-byte swizzle, the operand layout of kind::mxf8f6f4 for E2M1. The
-// transaction count of a box is its global bytes (64 per row).
-bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows);
+// Tensor map of packed E2M1 weights in tile order (moe_tile_mxfp4_weights),
+// read as rows64 rows of 128 elements (64 bytes each, contiguous; ptr 32-byte
+// aligned), box {128 elements, box_rows}: each 16 codes (8 bytes) land in the
+// low half of a 16-byte shared-memory slot, 128-byte swizzle, the operand
+// layout of kind::mxf8f6f4 for E2M1. A box's transaction count is its global
+// bytes (64 per row). The row of block (t, kb), row r is (t * nk + kb) * R + r,
+// R = 128 (one matrix) or 256 (a gate/up pair).
+bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t rows64, uint32_t box_rows);
 // Native MXFP8 grouped GEMM (gemm_mx.cu): block-scaled tcgen05 MMA, E4M3
 // activations (a + a_scale; GEMM-2 reads h + h_scale) and weights.
 cudaError_t gemm_mx_prepare_device();
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s);
+// MX GEMM-1 with 256 weight rows per MMA (gemm_mx_wide.cu); up to 512 groups.
+bool gemm_mx_wide_supported(const GroupedGemmArgs& a);
+cudaError_t gemm_mx_wide_prepare_device();
+cudaError_t launch_gemm_mx_wide_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 // The tiling launch_gemm_gate_up / launch_gemm_down will use (GemmMode).
 int gemm_pick_mode(const GroupedGemmArgs& a);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
@@ -165,6 +174,10 @@ cudaError_t launch_mx4_quantize(const void* in_bf16, int64_t rows, int cols, uin
 // Row-major E8M0 scales [rows, cols/32] -> atoms. s1 == nullptr: the atoms
 // of s0 (rows % 128 == 0). Else gate (s0) and up (s1) interleaved per 64 rows
 // (rows % 64 == 0), 2 * rows atom-matrix rows. cols % 128 == 0.
+// Packed E2M1 [rows, cols/2] (a gate/up pair with q1) -> the tile order of
+// moe_tile_mxfp4_weights.
+cudaError_t launch_tile_e2m1(const uint8_t* q0, const uint8_t* q1, int64_t rows, int cols, uint8_t* dst,
+                             cudaStream_t s);
 cudaError_t launch_pack_weight_scales(const uint8_t* s0, const uint8_t* s1, int64_t rows, int cols,
                                       uint8_t* out, cudaStream_t s);
 // Activation scales [src_rows, cols/32] -> atoms by token tile of each group

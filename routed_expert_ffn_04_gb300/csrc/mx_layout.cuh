@@ -25,4 +25,5 @@ __host__ __device__ constexpr int atom_byte(int r, int j) {
   return 16 * (r & 31) + 4 * (r >> 5) + j;
 }
 
+
 }  // namespace moe

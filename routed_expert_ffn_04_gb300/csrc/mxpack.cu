@@ -1,6 +1,7 @@
 // Scale atoms (mx_layout.cuh) for the block-scaled MXFP8 GEMM: packing of
 // row-major E8M0 weight scales, and the gather of activation scales into one
-// atom row-block per token tile of each expert group.
+// atom row-block per token tile of each expert group. Also the tile order of
+// packed E2M1 weights (the W4A8 routed experts).
 //
 // Weights ("腾讯混元 Hy3 在 CANN NPU 上的高性能推理部署与优化实战", section
 // 8.2: routed and shared expert Linears in MXFP8) are packed once, like their
@@ -122,7 +123,42 @@ __global__ void __launch_bounds__(kGatherThreads) gather_scale_atoms_kernel(
   }
 }
 
+// Packed E2M1 weights [rows, cols/2] -> tile order (moe_tile_mxfp4_weights):
+// per 128-row block t and 128-element K block kb one contiguous block at
+// (t * nk + kb): 128 rows of 64 bytes (q1 == nullptr, 8 KB), or for a gate
+// (q0) / up (q1) pair 16 KB: q0 rows 0-63, q1 rows 0-63, q0 rows 64-127, q1
+// rows 64-127 of the block. One thread per 16 bytes of the output.
+__global__ void __launch_bounds__(256) tile_e2m1_kernel(const uint4* __restrict__ q0, const uint4* __restrict__ q1,
+                                                        long long chunks, int nk, uint4* __restrict__ dst) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= chunks) return;
+  const int per_blk = q1 ? 1024 : 512;  // 16-byte chunks per block
+  const long long blk = i / per_blk;
+  const int within = (int)(i - blk * per_blk);
+  const long long t = blk / nk;
+  const int kb = (int)(blk - t * nk);
+  const uint4* src = q0;
+  int r = within >> 2;
+  if (q1) {
+    const int quarter = within >> 8;  // 64-row pieces: q0, q1, q0, q1
+    src = (quarter & 1) ? q1 : q0;
+    r = (quarter >> 1) * 64 + ((within & 255) >> 2);
+  }
+  // Source row: nk * 4 chunks of 16 bytes; this block's 64 bytes start at chunk 4 kb.
+  dst[i] = __ldg(src + (t * 128 + r) * (nk * 4) + kb * 4 + (within & 3));
+}
+
 }  // namespace
+
+cudaError_t launch_tile_e2m1(const uint8_t* q0, const uint8_t* q1, int64_t rows, int cols, uint8_t* dst,
+                             cudaStream_t s) {
+  const long long chunks = (q1 ? 2 : 1) * (long long)rows * cols / 32;  // bytes / 16
+  if (chunks == 0) return cudaSuccess;
+  tile_e2m1_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(q0), reinterpret_cast<const uint4*>(q1), chunks, cols / 128,
+      reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack_weight_scales(const uint8_t* s0, const uint8_t* s1, int64_t rows, int cols,
                                       uint8_t* out, cudaStream_t s) {

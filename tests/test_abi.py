@@ -128,5 +128,15 @@ def test_small_workspace_rejected(lib):
     assert rc == moe.MOE_ERR_INVALID_ARG
 
 
+def test_tile_mxfp4_argument_checks(lib):
+    P = ctypes.c_void_p
+    # rows % 128, cols % 128 and distinct buffers are checked before the handle.
+    assert lib.moe_tile_mxfp4_weights(None, P(256), None, 64, 256, P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_tile_mxfp4_weights(None, P(256), None, 128, 192, P(4096), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_tile_mxfp4_weights(None, P(256), None, 128, 256, P(256), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_tile_mxfp4_weights(None, P(256), P(512), 128, 256, P(512), None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_tile_mxfp4_weights(None, P(256), P(512), 128, 256, P(4096), None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_option_validation(lib):
     assert lib.moe_set_option(None, 0, 1) == moe.MOE_ERR_INVALID_ARG

@@ -59,6 +59,27 @@ def test_mxfp4_quantiser_bit_exact(handle):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 384), (1536 * 2, 4096)])
+def test_tile_order_is_the_stated_byte_permutation(handle, rows, cols):
+    # Tile order of one matrix: the 128-row x 128-element block (t, kb) is 8 KB
+    # at block t * (cols // 128) + kb, its rows 64 bytes apart. Of a gate/up
+    # pair: 16 KB per block, gate rows 0-63, up rows 0-63, gate rows 64-127, up
+    # rows 64-127. Stated here as reshapes / transposes of the row-major bytes.
+    g = torch.Generator().manual_seed(rows)
+    q0 = torch.randint(0, 256, (rows, cols // 2), dtype=torch.int32, generator=g).to(torch.uint8)
+    q1 = torch.randint(0, 256, (rows, cols // 2), dtype=torch.int32, generator=g).to(torch.uint8)
+    nt, nk = rows // 128, cols // 128
+    t = moe.tile_mxfp4(handle, q0.cuda())
+    tp = moe.tile_mxfp4(handle, q0.cuda(), q1.cuda())
+    torch.cuda.synchronize()
+    blocks0 = q0.numpy().reshape(nt, 128, nk, 64).transpose(0, 2, 1, 3)     # [t, kb, row, byte]
+    assert np.array_equal(t.cpu().numpy().reshape(-1), blocks0.reshape(-1))
+    halves0 = blocks0.reshape(nt, nk, 2, 64, 64)                            # [t, kb, half, row, byte]
+    halves1 = q1.numpy().reshape(nt, 128, nk, 64).transpose(0, 2, 1, 3).reshape(nt, nk, 2, 64, 64)
+    pair = np.stack([halves0, halves1], axis=3)                             # [t, kb, half, gate/up, row, byte]
+    assert np.array_equal(tp.cpu().numpy().reshape(-1), pair.reshape(-1))
+
+
 def _w4a8_weights_oracle(w):
     return {k: (oracle.mxfp4_quantize(v.cpu()) if k.startswith("w_") else oracle.mx_quantize(v.cpu()))
             for k, v in w.items()}
