@@ -478,14 +478,14 @@ __global__ void __launch_bounds__(Geo<SWAP, MODE, BN, GATHER>::THREADS, 1)
           const uint32_t st = base_u32 + rg.s * Gm::STAGE_BYTES;
           const uint32_t sA = st + (SWAP ? Gm::W_OFF : Gm::ACT_OFF);
           const uint32_t sB = st + (SWAP ? Gm::ACT_OFF : Gm::W_OFF);
+          // +32 bytes along K is +2 in a descriptor's start-address field.
+          const uint64_t da = sw128_kmajor_desc(sA), db = sw128_kmajor_desc(sB);
+          const uint64_t da2 = SWAP ? sw128_kmajor_desc(sA + Gm::kTileBytes) : 0;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accum = (kb | k) ? 1u : 0u;
-            const uint64_t bdesc = sw128_kmajor_desc(sB + k * 32);
-            umma_bf16(d, sw128_kmajor_desc(sA + k * 32), bdesc, kIdesc, accum);
-            if (SWAP)
-              umma_bf16(d + BN, sw128_kmajor_desc(sA + Gm::kTileBytes + k * 32), bdesc, kIdesc,
-                        accum);
+            umma_bf16(d, da + 2 * k, db + 2 * k, kIdesc, accum);
+            if (SWAP) umma_bf16(d + BN, da2 + 2 * k, db + 2 * k, kIdesc, accum);
           }
           issued = true;
           umma_commit(empty_bar(rg.s));

@@ -249,10 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t st = stage0 + rg.s * kStageBytes;
           const uint32_t sf = tmem_base + (uint32_t)(kSfCol0 + 8 * rg.s);
+          // +32 bytes along K is +2 in a descriptor's start-address field.
+          const uint64_t da = sw128_kmajor_desc(st), db = sw128_kmajor_desc(st + kTileBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            umma_mxf8(d, sw128_kmajor_desc(st + k * 32), sw128_kmajor_desc(st + kTileBytes + k * 32),
-                      idesc_mxf8_e4m3(128, 128, k, k) | kIdescFmt, sf, sf + 4, (kb | k) ? 1u : 0u);
+            umma_mxf8(d, da + 2 * k, db + 2 * k, idesc_mxf8_e4m3(128, 128, k, k) | kIdescFmt, sf, sf + 4,
+                      (kb | k) ? 1u : 0u);
           }
           issued = true;
           umma_commit(empty_bar(rg.s));

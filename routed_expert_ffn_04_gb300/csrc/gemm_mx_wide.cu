@@ -12,10 +12,10 @@
 // At N = 128 the MMA thread alone (4 MMAs, a commit, the waits) needed ~620
 // cycles per stage. So this kernel doubles the work per MMA and keeps every
 // role's per-stage work short:
-//   - the MMA thread waits on two barriers (weights + activations together,
-//     and the stage's scales), issues 4 MMAs from precomputed descriptors and
-//     one commit, which frees the weight stage, the activation stage and the
-//     TMEM scale slot at once (their rings are tied to the weight ring);
+//   - the MMA thread waits on one barrier per stage (weights, activations and
+//     the stage's scales in TMEM), issues 4 MMAs from precomputed descriptors
+//     and one commit, which frees the weight stage, the activation stage and
+//     the TMEM scale slot at once (their rings are tied to the weight ring);
 //   - with E2M1 weights in tile order (moe_tile_mxfp4_weights) a stage's 256
 //     weight rows are one contiguous 16 KB block and one TMA load;
 //   - scale atoms are fetched two stages per bulk copy, two groups ahead of
@@ -78,7 +78,7 @@ constexpr int wSfCol0 = wAccCols;         // TMEM scale slot s: wSfCol0 + 16 s (
 constexpr int wTmemCols = 512;
 constexpr int wMaxGroups = 512;
 constexpr int wTableBytes = 2 * (wMaxGroups + 8) * 4;  // tile starts + group row starts
-constexpr int wNumBars = 3 * wStagesB + 2 * wGroupSlots + 4;
+constexpr int wNumBars = 2 * wStagesB + 2 * wGroupSlots + 4;
 constexpr int wBarBytes = 256;
 // Shared memory: weight ring | activation ring | atom groups | tables | barriers.
 constexpr int wOffA = wStagesB * wBTile;
@@ -147,16 +147,17 @@ __global__ void __launch_bounds__(wThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + wNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  // full(s): stage s's weights and activations landed; empty(s): its MMAs are
-  // done (frees the weight stage, the activation stage of the same K stage
-  // and TMEM scale slot s); sfull(s): its scales are in TMEM slot s.
+  // full(s): stage s's weights and activations landed and its scales are in
+  // TMEM slot s (two arrivals: the weight producer's, with both producers'
+  // bytes, and the scale warp's commit); empty(s): its MMAs are done (frees
+  // the weight stage, the activation stage of the same K stage and TMEM scale
+  // slot s).
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (wStagesB + s); };
-  auto sfull = [&](int s) { return bar0 + 8u * (2 * wStagesB + s); };
   // gfull(g): atom group slot g landed; gfree(g): its copies into TMEM are done.
-  auto gfull = [&](int g) { return bar0 + 8u * (3 * wStagesB + g); };
-  auto gfree = [&](int g) { return bar0 + 8u * (3 * wStagesB + wGroupSlots + g); };
-  const uint32_t tfull_bar = bar0 + 8u * (3 * wStagesB + 2 * wGroupSlots);
+  auto gfull = [&](int g) { return bar0 + 8u * (2 * wStagesB + g); };
+  auto gfree = [&](int g) { return bar0 + 8u * (2 * wStagesB + wGroupSlots + g); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * wStagesB + 2 * wGroupSlots);
   const uint32_t tempty_bar = tfull_bar + 8u;
   const uint32_t drain_bar = tfull_bar + 16u;
   const uint32_t sdrain_bar = tfull_bar + 24u;
@@ -171,9 +172,8 @@ __global__ void __launch_bounds__(wThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < wStagesB; ++s) {
-      mbar_init(full(s), 1);  // the weight producer's arrival; both producers' bytes
+      mbar_init(full(s), 2);  // the weight producer's arrival (both producers' bytes) + the scale commit
       mbar_init(empty(s), 1);
-      mbar_init(sfull(s), 1);
     }
     for (int g = 0; g < wGroupSlots; ++g) {
       mbar_init(gfull(g), 1);
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(wThreads, 1)
           tmem_cp_32x128b_warpx4(sf + 8, src + wGroup * kAtomBytes);
           tmem_cp_32x128b_warpx4(sf + 12, src + 2 * wGroup * kAtomBytes);
           issued = true;
-          umma_commit(sfull(s));
+          umma_commit(full(s));
           if (last) {
             umma_commit(gfree(gs));  // the group slot may be reloaded once these copies are done
             ++ng;
@@ -397,8 +397,7 @@ __global__ void __launch_bounds__(wThreads, 1)
         for (int kb = 0; kb < n_k; ++kb, ++j) {
           const int s = j % wStagesB;
           const uint32_t ph = round_parity(j, wStagesB);
-          if (!mbar_wait_bounded(full(s), ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA, p.limit_ns) ||
-              !mbar_wait_bounded(sfull(s), ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
+          if (!mbar_wait_bounded(full(s), ph, abort_flag, p.status, MOE_DEV_TIMEOUT_MMA, p.limit_ns)) {
             ok = false;
             break;
           }
