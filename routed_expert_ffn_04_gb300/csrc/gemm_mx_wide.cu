@@ -37,10 +37,10 @@
 // Persistent, one CTA per SM, 384 threads:
 //   warp 0      weight producer: per 128-wide K stage the stage's weight rows
 //               (one box for E2M1 in tile order, four for row-major E4M3),
-//               5-stage ring; and the scale atoms of stage pairs two groups
+//               4-stage ring; and the scale atoms of stage pairs two groups
 //               ahead.
 //   warp 11     activation producer: the A tile (128 token rows), completing
-//               on the weight stage's barrier (3-stage ring; mostly L2 hits: a
+//               on the weight stage's barrier (4-stage ring; mostly L2 hits: a
 //               token tile is read by every weight tile of its expert).
 //   warp 2      scale warp: three tcgen05.cp per stage into the stage's slot.
 //   warp 1      TMEM allocator + MMA issuer: 4 MMAs (K = 32) per stage.
@@ -59,8 +59,9 @@
 namespace moe {
 namespace {
 
-constexpr int wStagesB = 5;               // weight ring; also the TMEM scale slots
-constexpr int wStagesA = 3;               // activation ring
+constexpr int wStagesB = 4;               // weight ring; also the TMEM scale slots
+constexpr int wStagesA = 4;               // activation ring (one slot per weight slot: measured
+                                          // faster than 5 + 3, the activation loads wait on L2 too)
 constexpr int wGroup = 2;                 // K stages per atom group (one bulk copy per atom kind)
 constexpr int wGroupSlots = 4;            // atom groups in shared memory
 constexpr int wGroupAhead = 2;            // groups between an atom group's load and its first stage
@@ -89,7 +90,7 @@ constexpr int wSmem = 1024 + wOffBars + wBarBytes;
 static_assert(wSmem <= 232448, "shared memory budget");
 static_assert(wSfCol0 + 16 * wStagesB <= wTmemCols, "TMEM budget");
 static_assert(wNumBars * 8 + 8 <= wBarBytes, "barrier area");
-static_assert(wStagesA < wStagesB, "an activation slot is freed by an earlier weight-ring phase");
+static_assert(wStagesA <= wStagesB, "an activation slot is freed by a weight-ring phase no later than its own");
 static_assert(wGroupAhead < wGroupSlots, "an atom group slot is reloaded only after its copies");
 static_assert(wThreads == 32 * (wProdAWarp + 1) && wEpiWarp0 + wEpiWarps == wProdAWarp, "warp roles");
 
