@@ -42,13 +42,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # its own algorithmic bytes (traffic grows with the bytes the launch must
 # move: the touched experts' weights, the activation rows, h). A value is
 # reported only while the GEMM sources still hash as they did for the capture.
-GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_sched.cuh", "ptx.cuh")
-GEMM1_TRAFFIC_SHA = "125e3a614070d27e"
+GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_mx_wide.cu", "gemm_sched.cuh", "ptx.cuh")
+GEMM1_TRAFFIC_SHA = "d27d9d82132dc968"
 GEMM1_TRAFFIC_RATIO = {
-    "decode": (1212221696 + 2967552) / 1213726720,   # E = 48
-    "prefill": (1169254144 + 191149824) / 1073741824,  # E = 32, A rows gathered from x
-    "mxfp8": (692713728 + 24632320) / 718012416,     # E = 48
-    "mxfp4": (390618880 + 22769920) / 416022528,     # E = 48
+    "decode": (1212224256 + 3239424) / 1213726720,     # E = 48
+    "prefill": (1165653760 + 190913024) / 1073741824,  # E = 32, A rows gathered from x
+    "mxfp8": (692773120 + 25095936) / 718012416,       # E = 48
+    "mxfp4": (390632704 + 21934336) / 416022528,       # E = 48, 256-row weight tile
 }
 
 
