@@ -144,10 +144,11 @@ typedef enum {
    * gather fused into the grouped GEMM) and x_perm is not written; 0 = the
    * permutation writes x_perm and GEMM-1 reads it. The result is the same. */
   MOE_OPT_GATHER_A = 5,
-  /* Weight rows per MMA of the MX (MXFP8, W4A8) grouped GEMM-1: 0 = automatic
-   * (default: 256 for E2M1 weights, 128 for E4M3), 1 = 128 (gate 64 + up 64,
-   * double-buffered accumulators), 2 = 256 (gate 128 + up 128, one
-   * accumulator). The result is the same up to fp32 summation order. */
+  /* Weight rows per MMA of the MX (MXFP8, W4A8) grouped GEMMs: 0 = automatic
+   * (default: 256 for E2M1 weights, 128 for E4M3), 1 = 128
+   * (GEMM-1 gate 64 + up 64; double-buffered accumulators), 2 = 256 (GEMM-1
+   * gate 128 + up 128; GEMM-2 when H % 256 == 0; one accumulator). The result
+   * is the same up to fp32 summation order. */
   MOE_OPT_MX_TILE = 6
 } moe_option_t;
 

@@ -127,7 +127,16 @@ __device__ __forceinline__ void store_h_block(const uint32_t (&g)[32], const uin
 // (n = 0, 1, ...) when stage n * depth + slot completes.
 __device__ __forceinline__ uint32_t round_parity(int stage, int depth) { return (uint32_t)(stage / depth) & 1u; }
 
-template <bool W4>
+// 32 fp32 values of a y row, as eight 16-byte stores.
+__device__ __forceinline__ void store_y_cols(const uint32_t (&v)[32], float* dst) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    d[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                       __uint_as_float(v[4 * j + 3]));
+}
+
+template <int MODE, bool W4>
 __global__ void __launch_bounds__(wThreads, 1)
     grouped_gemm_mx_wide_kernel(const __grid_constant__ CUtensorMap map_act,
                                 const __grid_constant__ CUtensorMap map_w0,
@@ -164,7 +173,9 @@ __global__ void __launch_bounds__(wThreads, 1)
   const uint32_t sdrain_bar = tfull_bar + 24u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_wt = p.N / 128;  // h columns per tile: 128 (N % 128 == 0)
+  // Output columns per tile: GEMM-1 128 of h (N = I % 128 == 0), GEMM-2 256 of y (N = H % 256 == 0).
+  constexpr int kCols = MODE == 0 ? 128 : 256;
+  const int n_wt = p.N / kCols;
   fill_row_start(p, row_start, threadIdx.x, wThreads);
   for (int g = threadIdx.x; g < p.G; g += wThreads) {
     int r0, nr;
@@ -244,7 +255,9 @@ __global__ void __launch_bounds__(wThreads, 1)
         const int cnt = n_k - g_kb < wGroup ? n_k - g_kb : wGroup;
         const uint32_t bytes = (uint32_t)cnt * kAtomBytes;
         const long long a_blk = tile_start[g_ti.g] / n_wt + g_ti.tt;
-        const long long b_blk = (long long)g_ti.g * (2 * p.N / 128) + 2 * g_ti.wt;  // atoms b_blk, b_blk + 1
+        // Weight atoms b_blk, b_blk + 1: GEMM-1 the gate/up atom matrix (2N rows per
+        // group), GEMM-2 the down atoms (N rows per group).
+        const long long b_blk = (long long)g_ti.g * ((MODE == 0 ? 2 : 1) * p.N / 128) + 2 * g_ti.wt;
         const uint8_t* a_atom = p.s_act + (a_blk * n_k + g_kb) * kAtomBytes;
         const uint8_t* b_atom = p.s_w0 + (b_blk * n_k + g_kb) * kAtomBytes;
         const uint32_t dst = sm0 + wOffSf + gs * wGroupBytes;
@@ -270,8 +283,10 @@ __global__ void __launch_bounds__(wThreads, 1)
       int j = 0;  // stage
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const TileInfo ti = decode_tile_s<128>(p.G, tile_start, row_start, tile);
-        const int w_row = ti.g * p.N + ti.wt * 128;
-        const int t = ti.g * n_wt + ti.wt;  // 128-row block of the gate/up pair in tile order
+        const int w_row = ti.g * p.N + ti.wt * kCols;
+        // Tile order: GEMM-1 the gate/up pair block t (256 rows), GEMM-2 the
+        // 128-row down blocks t and t + 1.
+        const int t = MODE == 0 ? ti.g * n_wt + ti.wt : (ti.g * p.N + ti.wt * kCols) / 128;
         for (int kb = 0; kb < n_k; ++kb, ++j) {
           if (kb % wGroup == 0 && !load_group()) {
             ok = false;
@@ -287,13 +302,22 @@ __global__ void __launch_bounds__(wThreads, 1)
           mbar_arrive_expect_tx(fb, kTxStage);
           const uint32_t st = sm0 + s * wBTile;
           if (W4) {
-            tma_load_2d_hint(st, &map_w0, fb, 0, (t * n_k + kb) * 256, pol);
+            if (MODE == 0) {
+              tma_load_2d_hint(st, &map_w0, fb, 0, (t * n_k + kb) * 256, pol);
+            } else {
+              tma_load_2d_hint(st, &map_w0, fb, 0, (t * n_k + kb) * 128, pol);
+              tma_load_2d_hint(st + 2 * wBox, &map_w0, fb, 0, ((t + 1) * n_k + kb) * 128, pol);
+            }
           } else {
+            // Row-major E4M3, four 64-row boxes: GEMM-1 gate, up, gate, up (64 rows
+            // each, the atoms' order); GEMM-2 256 consecutive down rows.
             const int kx = kb * 128;
+            const CUtensorMap* m1 = MODE == 0 ? &map_w1 : &map_w0;
+            const int r1 = MODE == 0 ? 0 : 64;
             tma_load_2d_hint(st, &map_w0, fb, kx, w_row, pol);
-            tma_load_2d_hint(st + wBox, &map_w1, fb, kx, w_row, pol);
-            tma_load_2d_hint(st + 2 * wBox, &map_w0, fb, kx, w_row + 64, pol);
-            tma_load_2d_hint(st + 3 * wBox, &map_w1, fb, kx, w_row + 64, pol);
+            tma_load_2d_hint(st + wBox, m1, fb, kx, w_row + r1, pol);
+            tma_load_2d_hint(st + 2 * wBox, &map_w0, fb, kx, w_row + (MODE == 0 ? 64 : 128), pol);
+            tma_load_2d_hint(st + 3 * wBox, m1, fb, kx, w_row + (MODE == 0 ? 64 : 192), pol);
           }
           Ring r;
           r.s = s;
@@ -428,7 +452,7 @@ __global__ void __launch_bounds__(wThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                    // TMEM lane quarter this warp may read
-    const int hh = (warp - wEpiWarp0) >> 2;    // which 128 accumulator columns (64 h columns)
+    const int hh = (warp - wEpiWarp0) >> 2;    // which 128 accumulator columns
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       int ok = 1;
@@ -438,7 +462,8 @@ __global__ void __launch_bounds__(wThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      // Accumulator columns of this warp: gate 64 (two blocks of 32), then up 64.
+      // Accumulator columns of this warp: GEMM-1 gate 64 (two blocks of 32), then
+      // up 64; GEMM-2 128 consecutive y columns.
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(hh * 128);
       uint32_t g0[32], g1[32], u0[32], u1[32];
       tmem_ld_32x32b_x32(tb, g0);
@@ -451,7 +476,15 @@ __global__ void __launch_bounds__(wThreads, 1)
       if (lane == 0) mbar_arrive(tempty_bar);  // the MMA may overwrite the accumulator now
       const TileInfo ti = decode_tile_s<128>(p.G, tile_start, row_start, tile);
       const int r = ti.tt * 128 + q * 32 + lane;
-      if (r < ti.nrows) {
+      if (MODE == 1) {
+        if (r < ti.nrows) {
+          float* yrow = static_cast<float*>(p.out) + (size_t)(ti.row0 + r) * p.N + ti.wt * kCols + hh * 128;
+          store_y_cols(g0, yrow);
+          store_y_cols(g1, yrow + 32);
+          store_y_cols(u0, yrow + 64);
+          store_y_cols(u1, yrow + 96);
+        }
+      } else if (r < ti.nrows) {
         const long long a_blk = tile_start[ti.g] / n_wt + ti.tt;
         uint8_t* h_atoms = p.out_scale + a_blk * (p.N / 128) * kAtomBytes;
         const int col = ti.wt * 128 + hh * 64;
@@ -473,55 +506,70 @@ __global__ void __launch_bounds__(wThreads, 1)
   }
 }
 
-template <bool W4>
+template <int MODE, bool W4>
 cudaError_t run_gemm_mx_wide(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.rows == 0 || a.G == 0) return cudaSuccess;
-  if (a.H % 128 || a.I % 128 || a.G > wMaxGroups) return cudaErrorInvalidValue;
+  if (a.H % 128 || a.I % 128 || a.G > wMaxGroups || (MODE == 1 && a.H % 256)) return cudaErrorInvalidValue;
   const int G = a.offsets ? a.G : 1;
+  const int Kdim = MODE == 0 ? a.H : a.I;
+  const int N = MODE == 0 ? a.I : a.H;
+  const void* act = MODE == 0 ? a.a : a.h;
   CUtensorMap m_act, m_w0, m_w1;
-  bool maps_ok = make_tmap_u8(&m_act, a.a, a.H, a.rows, 128);
-  if (W4) {  // the gate/up pair in tile order: one 256-row box per stage
-    maps_ok = maps_ok && make_tmap_e2m1(&m_w0, a.w_gate, 2ull * G * a.I * (a.H / 128), 256);
+  bool maps_ok = make_tmap_u8(&m_act, act, Kdim, a.rows, 128);
+  if (W4) {  // tile order: GEMM-1 the gate/up pair (256-row boxes), GEMM-2 down (128-row boxes)
+    maps_ok = maps_ok && (MODE == 0 ? make_tmap_e2m1(&m_w0, a.w_gate, 2ull * G * N * (Kdim / 128), 256)
+                                    : make_tmap_e2m1(&m_w0, a.w_down, (uint64_t)G * N * (Kdim / 128), 128));
     m_w1 = m_w0;
+  } else if (MODE == 0) {
+    maps_ok = maps_ok && make_tmap_u8(&m_w0, a.w_gate, Kdim, (uint64_t)G * N, 64) &&
+              make_tmap_u8(&m_w1, a.w_up, Kdim, (uint64_t)G * N, 64);
   } else {
-    maps_ok = maps_ok && make_tmap_u8(&m_w0, a.w_gate, a.H, (uint64_t)G * a.I, 64) &&
-              make_tmap_u8(&m_w1, a.w_up, a.H, (uint64_t)G * a.I, 64);
+    maps_ok = maps_ok && make_tmap_u8(&m_w0, a.w_down, Kdim, (uint64_t)G * N, 64);
+    m_w1 = m_w0;
   }
   if (!maps_ok) return cudaErrorInvalidValue;
   KParams p = {};
   p.offsets = a.offsets;
   p.G = G;
   p.rows = a.rows;
-  p.num_kb = a.H / 64;
-  p.N = a.I;
-  p.out = a.h;
+  p.num_kb = Kdim / 64;
+  p.N = N;
+  p.out = MODE == 0 ? a.h : static_cast<void*>(a.y);
   p.status = a.status;
   p.limit_ns = a.wait_limit_ns;
-  p.s_w0 = a.s_gate;
-  p.s_act = a.a_scale;
-  p.out_scale = a.h_scale;
-  const long long n_wt = a.I / 128;
+  p.s_w0 = MODE == 0 ? a.s_gate : a.s_down;
+  p.s_act = MODE == 0 ? a.a_scale : a.h_scale;
+  p.out_scale = MODE == 0 ? a.h_scale : nullptr;
+  const long long n_wt = N / (MODE == 0 ? 128 : 256);
   const long long max_tiles = n_wt * ((a.rows + 127) / 128 + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
-  grouped_gemm_mx_wide_kernel<W4><<<grid, wThreads, wSmem, s>>>(m_act, m_w0, m_w1, p);
+  grouped_gemm_mx_wide_kernel<MODE, W4><<<grid, wThreads, wSmem, s>>>(m_act, m_w0, m_w1, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-bool gemm_mx_wide_supported(const GroupedGemmArgs& a) { return (a.offsets ? a.G : 1) <= wMaxGroups; }
+bool gemm_mx_wide_supported(const GroupedGemmArgs& a, int mode) {
+  return (a.offsets ? a.G : 1) <= wMaxGroups && (mode == 0 || a.H % 256 == 0);
+}
 
 cudaError_t gemm_mx_wide_prepare_device() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             wSmem);
-  return e;
+  const cudaError_t errs[] = {
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem)};
+  for (cudaError_t e : errs)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm_mx_wide_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
-  return a.w4 ? run_gemm_mx_wide<true>(a, s) : run_gemm_mx_wide<false>(a, s);
+  return a.w4 ? run_gemm_mx_wide<0, true>(a, s) : run_gemm_mx_wide<0, false>(a, s);
+}
+
+cudaError_t launch_gemm_mx_wide_down(const GroupedGemmArgs& a, cudaStream_t s) {
+  return a.w4 ? run_gemm_mx_wide<1, true>(a, s) : run_gemm_mx_wide<1, false>(a, s);
 }
 
 }  // namespace moe

@@ -135,10 +135,12 @@ bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, uint64_t rows64, uint32_t b
 cudaError_t gemm_mx_prepare_device();
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s);
-// MX GEMM-1 with 256 weight rows per MMA (gemm_mx_wide.cu); up to 512 groups.
-bool gemm_mx_wide_supported(const GroupedGemmArgs& a);
+// MX GEMMs with 256 weight rows per MMA (gemm_mx_wide.cu): up to 512 groups;
+// GEMM-2 (mode 1) needs H % 256 == 0.
+bool gemm_mx_wide_supported(const GroupedGemmArgs& a, int mode);
 cudaError_t gemm_mx_wide_prepare_device();
 cudaError_t launch_gemm_mx_wide_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_mx_wide_down(const GroupedGemmArgs& a, cudaStream_t s);
 // The tiling launch_gemm_gate_up / launch_gemm_down will use (GemmMode).
 int gemm_pick_mode(const GroupedGemmArgs& a);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);

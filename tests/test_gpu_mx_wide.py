@@ -1,5 +1,6 @@
-"""GPU parity of the wide-tile MX GEMM-1 (MOE_OPT_MX_TILE = 2: 256 weight rows,
-gate 128 + up 128, per block-scaled MMA, one accumulator) for MXFP8 and W4A8
+"""GPU parity of the wide-tile MX GEMMs (MOE_OPT_MX_TILE = 2: 256 weight rows
+per block-scaled MMA, one accumulator; GEMM-1 gate 128 + up 128, GEMM-2 256
+columns of y when H % 256 == 0, else the 128-row GEMM-2) for MXFP8 and W4A8
 weights, against the oracle's MX SwiGLU MLP ("腾讯混元 Hy3 在 CANN NPU 上的高性能
 推理部署与优化实战", section 8.2): ragged groups (empty groups, single rows, more
 than one token tile), I of one and of several wide tiles, and the full MXFP8 and
