@@ -43,12 +43,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # move: the touched experts' weights, the activation rows, h). A value is
 # reported only while the GEMM sources still hash as they did for the capture.
 GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_mx_wide.cu", "gemm_sched.cuh", "ptx.cuh")
-GEMM1_TRAFFIC_SHA = "d27d9d82132dc968"
+GEMM1_TRAFFIC_SHA = "08be95b58d284556"
 GEMM1_TRAFFIC_RATIO = {
-    "decode": (1212224256 + 3239424) / 1213726720,     # E = 48
-    "prefill": (1165653760 + 190913024) / 1073741824,  # E = 32, A rows gathered from x
-    "mxfp8": (692773120 + 25095936) / 718012416,       # E = 48
-    "mxfp4": (390632704 + 21934336) / 416022528,       # E = 48, 256-row weight tile
+    "decode": (1212235264 + 3315200) / 1213726720,     # E = 48
+    "prefill": (1164402432 + 191267840) / 1073741824,  # E = 32, A rows gathered from x
+    "mxfp8": (692628992 + 24681472) / 718012416,       # E = 48
+    "mxfp4": (390629632 + 21867008) / 416022528,       # E = 48, 256-row weight tile
 }
 
 
