@@ -165,3 +165,24 @@ def test_wide_layer_full_size_tile_edges(handle, dtype):
     ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _w_oracle(w, w4), K=shape.K, scaling=shape.scaling,
                                   tokens=tokens, w4=w4)
     _check(out.float().cpu().numpy()[tokens], ref, f"{dtype} workload, wide tile")
+
+
+def test_many_groups_fall_back_to_the_128_row_kernels(handle):
+    # More than 512 groups: both W4A8 GEMMs take the 128-row kernels, which read
+    # the same tile-ordered weights (gate/up pair for GEMM-1, down for GEMM-2).
+    H, I = 256, 128
+    sizes = [0] * 600
+    for gi, n in ((3, 5), (200, 130), (511, 1), (512, 40), (599, 77)):
+        sizes[gi] = n
+    G, offsets, a, wg, wu, wd = _operands(H, I, sizes, 24)
+    aq, as_ = moe.quantize_mx(handle, a.cuda())
+    pw = _quantised_weights(handle, wg, wu, wd, True)
+    y = _run_gemm(handle, 0, aq, as_, offsets, pw, H, I, G, moe.MOE_MXFP4_W4A8)
+    xq, xs = oracle.mx_quantize(a)
+    q = oracle.mxfp4_quantize
+    for gi in range(G):
+        r0, r1 = offsets[gi], offsets[gi + 1]
+        if r1 == r0:
+            continue
+        ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], q(wg[gi]), q(wu[gi]), q(wd[gi]), w4=True)
+        _check(y[r0:r1], ref, f"group {gi} ({r1 - r0} rows)")
