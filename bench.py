@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "skewed", "mxfp8", "mxfp4"])
+    ap.add_argument("--dtype", default=None, choices=["bf16", "mxfp8", "mxfp4"],
+                    help="the workload's shape with these operands (mxfp4: W4A8) instead of its own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="time eager layer calls; by default one captured call is replayed as a CUDA graph")
@@ -435,6 +437,8 @@ def run_ours(args):
     shape = synth.WORKLOADS[args.workload]
     if args.experts:
         shape = shape.with_(E=args.experts)
+    if args.dtype:
+        shape = shape.with_(dtype=args.dtype)
     moe.load()  # fails loudly when the library is not built
 
     x, logits = synth.make_activations(shape, device=dev, seed=rank)
@@ -557,9 +561,13 @@ def run_ours(args):
     else:
         achieved = work["gemm1_flops"] / (g1_ms * 1e-3) / 1e12
         peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        if shape.dtype != "bf16":  # MX operands run at the fp8 rate: the measured bf16 peak x 2 (nominal ratio)
+            peak *= 2.0
+            peak_src += " x 2 (fp8 / bf16 nominal ratio)"
         unit = "TFLOP/s"
     traffic = None
-    if (args.workload in GEMM1_TRAFFIC_RATIO and not args.experts and not args.gated and not args.shared_fold
+    if (args.workload in GEMM1_TRAFFIC_RATIO and not args.experts and not args.dtype and not args.gated
+            and not args.shared_fold
             and args.gemm_mode == 0 and source_sha(GEMM1_TRAFFIC_SOURCES) == GEMM1_TRAFFIC_SHA):
         traffic = int(round(GEMM1_TRAFFIC_RATIO[args.workload] * work["gemm1_bytes"]))
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
@@ -592,7 +600,8 @@ def run_ours(args):
         "data": "synthetic (seeded: x~N(0,1), logits~N(0,1), weights~N(0,0.02) bf16, random init)",
         "config": {
             "workload": (f"Hy3-shape {args.workload} MoE layer" if args.workload != "tiny" else "tiny MoE layer")
-                        + (f" with E={shape.E}" if args.experts else ""),
+                        + (f" with E={shape.E}" if args.experts else "")
+                        + (f", {args.dtype} operands" if args.dtype else ""),
             "T": shape.T, "H": shape.H, "E": shape.E, "K": shape.K, "I": shape.I, "I_shared": shape.I_shared,
             "scaling": shape.scaling, "route_norm": shape.route_norm, "skewed_logits": shape.skew,
             "l2": f"inputs larger than L2: {work['layer_bytes'] / 1e9:.2f} GB of weights+activations per step",
@@ -674,6 +683,8 @@ def run_reference(args):
     if rank != 0:
         return
     shape = synth.WORKLOADS[args.workload]
+    if args.dtype:
+        shape = shape.with_(dtype=args.dtype)
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     x, logits = synth.make_activations(shape, device=dev, seed=0)
     w = synth.make_weights(shape, device=dev, seed=0)
@@ -703,7 +714,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64" + (f" on {shape.dtype} operands" if shape.dtype != "bf16" else ""),
         "data": "synthetic (same seeds as the CUDA arm)",
-        "config": {"workload": f"Hy3-shape {args.workload} MoE layer", "T": shape.T, "H": shape.H, "E": shape.E,
+        "config": {"workload": f"Hy3-shape {args.workload} MoE layer" + (f", {args.dtype} operands" if args.dtype else ""),
+                   "T": shape.T, "H": shape.H, "E": shape.E,
                    "K": shape.K, "I": shape.I, "I_shared": shape.I_shared},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": f"{n} token(s) of the {args.workload} workload per step through the fp64 oracle"},

@@ -153,3 +153,15 @@ def test_w4a8_layer_full_size_tile_edges(handle):
     ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _w4a8_weights_oracle(w), K=shape.K, scaling=shape.scaling,
                                   tokens=tokens, w4=True)
     _check(out.float().cpu().numpy()[tokens], ref, "mxfp4 workload")
+
+
+def test_w4a8_layer_decode_shape_all_tokens(handle):
+    # The decode shape (T=64, E=192, K=8) with W4A8 routed experts: about three
+    # rows per expert, so nearly every 128-row token tile is a partial one.
+    shape = synth.WORKLOADS["decode"].with_(dtype="mxfp4")
+    x, logits = synth.make_activations(shape, device="cuda", seed=3)
+    w = synth.make_weights(shape, device="cuda", seed=3)
+    out = _run_layer(shape, x, logits, w)
+    ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _w4a8_weights_oracle(w), K=shape.K, scaling=shape.scaling,
+                                  w4=True)
+    _check(out.float().cpu().numpy(), ref, "decode shape w4a8")
