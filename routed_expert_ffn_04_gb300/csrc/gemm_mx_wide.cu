@@ -1,9 +1,10 @@
-// Step 3's first GEMM in MX formats with a wide weight tile: the same
-// product as grouped_gemm_mx_kernel<0, W4> (gemm_mx.cu; "腾讯混元 Hy3 在 CANN
-// NPU 上的高性能推理部署与优化实战", section 8.2: W8A8 MXFP8 and the W4A8
-// recipe with MXFP4 routed weights), h = silu(x Wg^T) * (x Wu^T) re-quantised
-// to MXFP8 per 32 along I, but each MMA covers N = 256 weight rows (128 gate
-// + 128 up, 128 columns of h) instead of 128.
+// Step 3's GEMMs in MX formats with a wide weight tile: the same products as
+// grouped_gemm_mx_kernel<MODE, W4> (gemm_mx.cu; "腾讯混元 Hy3 在 CANN NPU 上的
+// 高性能推理部署与优化实战", section 8.2: W8A8 MXFP8 and the W4A8 recipe with
+// MXFP4 routed weights), but each MMA covers N = 256 weight rows instead of 128:
+//   MODE 0 (GEMM-1): gate 128 + up 128 rows, h = silu(x Wg^T) * (x Wu^T) for
+//                    128 columns of h, re-quantised to MXFP8 per 32 along I;
+//   MODE 1 (GEMM-2): 256 rows of W_down, y = h Wd^T for 256 columns, fp32.
 //
 // What sets the pace of these kernels is how much each issuing thread does
 // per K stage: every tcgen05 instruction, barrier wait and TMA issue costs
@@ -44,8 +45,9 @@
 //               token tile is read by every weight tile of its expert).
 //   warp 2      scale warp: three tcgen05.cp per stage into the stage's slot.
 //   warp 1      TMEM allocator + MMA issuer: 4 MMAs (K = 32) per stage.
-//   warps 3-10  epilogue: warp w reads TMEM lane quarter w % 4, h columns
-//               64 * ((w - 3) / 4) .. +63 of the tile.
+//   warps 3-10  epilogue: warp w reads TMEM lane quarter w % 4 and accumulator
+//               columns 128 * ((w - 3) / 4) .. +127: GEMM-1 h columns 64 of
+//               them, GEMM-2 128 y columns, stored from registers.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
