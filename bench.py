@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # move: the touched experts' weights, the activation rows, h). A value is
 # reported only while the GEMM sources still hash as they did for the capture.
 GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_mx_wide.cu", "gemm_sched.cuh", "ptx.cuh")
-GEMM1_TRAFFIC_SHA = "08be95b58d284556"
+GEMM1_TRAFFIC_SHA = "5a58e536a0c3b329"
 GEMM1_TRAFFIC_RATIO = {
     "decode": (1212235264 + 3315200) / 1213726720,     # E = 48
     "prefill": (1164402432 + 191267840) / 1073741824,  # E = 32, A rows gathered from x
