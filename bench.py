@@ -42,13 +42,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # its own algorithmic bytes (traffic grows with the bytes the launch must
 # move: the touched experts' weights, the activation rows, h). A value is
 # reported only while the GEMM sources still hash as they did for the capture.
-GEMM1_TRAFFIC_SOURCES = ("gemm.cu", "gemm_mx.cu", "gemm_mx_wide.cu", "gemm_sched.cuh", "ptx.cuh")
-GEMM1_TRAFFIC_SHA = "5a58e536a0c3b329"
-GEMM1_TRAFFIC_RATIO = {
-    "decode": (1212235264 + 3315200) / 1213726720,     # E = 48
-    "prefill": (1164402432 + 191267840) / 1073741824,  # E = 32, A rows gathered from x
-    "mxfp8": (692628992 + 24681472) / 718012416,       # E = 48
-    "mxfp4": (390629632 + 21867008) / 416022528,       # E = 48, 256-row weight tile
+# Per workload: the sources of its GEMM-1 kernel, their hash when captured, and
+# the captured ratio of traffic to algorithmic bytes.
+GEMM1_TRAFFIC = {
+    "decode": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1212235264 + 3315200) / 1213726720),      # E = 48
+    "prefill": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1164402432 + 191267840) / 1073741824),  # E = 32, A gathered
+    "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "02a418cdc801d075", (692628992 + 24681472) / 718012416),       # E = 48
+    "mxfp4": (('gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "fb1710b0057f2698", (390629632 + 21867008) / 416022528),  # E = 48, 256-row tile
 }
 
 
@@ -566,10 +566,10 @@ def run_ours(args):
             peak_src += " x 2 (fp8 / bf16 nominal ratio)"
         unit = "TFLOP/s"
     traffic = None
-    if (args.workload in GEMM1_TRAFFIC_RATIO and not args.experts and not args.dtype and not args.gated
-            and not args.shared_fold
-            and args.gemm_mode == 0 and source_sha(GEMM1_TRAFFIC_SOURCES) == GEMM1_TRAFFIC_SHA):
-        traffic = int(round(GEMM1_TRAFFIC_RATIO[args.workload] * work["gemm1_bytes"]))
+    if (args.workload in GEMM1_TRAFFIC and not args.experts and not args.dtype and not args.gated
+            and not args.shared_fold and args.gemm_mode == 0
+            and source_sha(GEMM1_TRAFFIC[args.workload][0]) == GEMM1_TRAFFIC[args.workload][1]):
+        traffic = int(round(GEMM1_TRAFFIC[args.workload][2] * work["gemm1_bytes"]))
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     # route 1; permute 1 (one block up to 16384 pairs, else 3) + row gather 1;
