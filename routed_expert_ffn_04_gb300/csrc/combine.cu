@@ -9,12 +9,11 @@
 // Two forms with the same arithmetic (sum over k ascending in fp32, one
 // bf16 rounding), chosen by the token count:
 //   - many tokens: one block per token (grid-stride), each thread owns 4
-//     consecutive columns at a time and reads them with 16-byte loads; the
-//     grid is full and HBM is the bound;
+//     consecutive columns at a time and reads them with 16-byte loads;
 //   - few tokens (fewer than two blocks per SM): a work unit is (token, chunk
-//     of 4 * blockDim columns), and each thread loads the K rows' vectors in
-//     batches of 8 before adding them, so that the few blocks keep enough
-//     loads in flight.
+//     of 4 * blockDim columns), so that the few tokens still fill the grid.
+// Both load the K rows' vectors of a column chunk in batches of 8 before
+// adding them, so each thread has several loads in flight.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,6 +25,47 @@ namespace {
 
 constexpr int kMaxK = 32;
 constexpr int kSms = 152;  // grid sizing
+constexpr int kBatch = 8;  // row loads in flight per thread
+
+// out[t, 4c .. 4c+3] from the token's K rows (sp: permuted row or -1, sw:
+// weight) and its shared-expert row.
+__device__ __forceinline__ void combine_chunk(const float* __restrict__ y_perm,
+                                              const float* __restrict__ shared_out, const float* sw,
+                                              const int32_t* sp, int t, int K, int H, int c,
+                                              __nv_bfloat16* __restrict__ out) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < K; k0 += kBatch) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int p = (k0 + j < K) ? sp[k0 + j] : -1;
+      v[j] = p >= 0 ? __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)p * H) + c)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (k0 + j >= K || sp[k0 + j] < 0) continue;
+      const float w = sw[k0 + j];
+      acc.x = fmaf(w, v[j].x, acc.x);
+      acc.y = fmaf(w, v[j].y, acc.y);
+      acc.z = fmaf(w, v[j].z, acc.z);
+      acc.w = fmaf(w, v[j].w, acc.w);
+    }
+  }
+  if (shared_out) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(shared_out + (size_t)t * H) + c);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = pk;
+}
 
 __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restrict__ y_perm,
                                                       const float* __restrict__ topk_w,
@@ -33,7 +73,6 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
                                                       const float* __restrict__ shared_out, int T,
                                                       int K, int H, __nv_bfloat16* __restrict__ out,
                                                       int* status) {
-  constexpr int kBatch = 8;
   __shared__ float sw[kMaxK];
   __shared__ int32_t sp[kMaxK];
   const int TK = T * K;
@@ -58,38 +97,7 @@ __global__ void __launch_bounds__(256) combine_split_kernel(const float* __restr
     }
     __syncthreads();
     if (c >= H4) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < K; k0 += kBatch) {
-      float4 v[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int p = (k0 + j < K) ? sp[k0 + j] : -1;
-        v[j] = p >= 0 ? __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)p * H) + c)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        if (k0 + j >= K || sp[k0 + j] < 0) continue;
-        const float w = sw[k0 + j];
-        acc.x = fmaf(w, v[j].x, acc.x);
-        acc.y = fmaf(w, v[j].y, acc.y);
-        acc.z = fmaf(w, v[j].z, acc.z);
-        acc.w = fmaf(w, v[j].w, acc.w);
-      }
-    }
-    if (shared_out) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(shared_out + (size_t)t * H) + c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = pk;
+    combine_chunk(y_perm, shared_out, sw, sp, t, K, H, c, out);
   }
 }
 
@@ -118,32 +126,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       sw[threadIdx.x] = w;
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < H4; c += blockDim.x) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < K; ++k) {
-        const int p = sp[k];
-        if (p < 0) continue;
-        const float w = sw[k];
-        const float4 v = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)p * H) + c);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-      if (shared_out) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(shared_out + (size_t)t * H) + c);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = pk;
-    }
+    for (int c = threadIdx.x; c < H4; c += blockDim.x) combine_chunk(y_perm, shared_out, sw, sp, t, K, H, c, out);
   }
 }
 
