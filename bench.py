@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--dtype", default=None, choices=["bf16", "mxfp8", "mxfp4"],
                     help="the workload's shape with these operands (mxfp4: W4A8) instead of its own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="with the default decode workload, skip the companion prefill measurement")
     ap.add_argument("--eager", action="store_true",
                     help="time eager layer calls; by default one captured call is replayed as a CUDA graph")
     ap.add_argument("--graph", action="store_true", help="(the default) time CUDA-graph replays")
@@ -301,6 +303,62 @@ def time_graph(call, args, main, dev, world):
     torch.cuda.synchronize()
     barrier(world)
     return g0.elapsed_time(g1) / args.steps
+
+
+def measure_prefill(moe, synth, w, dev, main, peaks):
+    """The metric's second half (TFLOP/s at prefill) measured in the same run
+    as the decode line: the Hy3-shape prefill layer (T=8192) on the decode
+    workload's weights (the same shapes and seed), CUDA-graph replays and
+    stage-timed eager calls, with its own clock samples."""
+    import types
+
+    import torch
+
+    shape = synth.WORKLOADS["prefill"]
+    x, logits = synth.make_activations(shape, device=dev, seed=0)
+    layer = moe.MoELayer(shape, w, device=dev.index)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((shape.T, shape.K), dtype=torch.int32, device=dev)
+    tw = torch.empty((shape.T, shape.K), dtype=torch.float32, device=dev)
+    moe.route(layer.handle, layer.cfg, logits, idx, tw)
+    counts = torch.bincount(idx.flatten().long(), minlength=shape.E).cpu().numpy()
+    work = algorithmic_work(shape, counts, gathered=True)
+
+    def call():
+        layer(x, logits, out)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 1)
+    for _ in range(10):
+        call()
+    torch.cuda.synchronize()
+    stage_ms, _ = layer.handle.stage_times()
+    layer.handle.set_option(moe.MOE_OPT_STAGE_TIMING, 0)
+    ms = time_graph(call, types.SimpleNamespace(steps=30, warmup=5), main, dev, 1)
+    clocks = sampler.stop()
+    if layer.handle.device_status() != 0:
+        raise RuntimeError("device status set during the prefill measurement")
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    burst = float(peaks["bf16_tflops"])
+    g1 = work["gemm1_flops"] / (stage_ms["gemm_gate_up"] * 1e-3) / 1e12
+    lay = work["flops"] / (ms * 1e-3) / 1e12
+    return {
+        "workload": f"Hy3-shape prefill MoE layer (T={shape.T}) on the decode weights",
+        "metric": "tokens/s; TFLOP/s vs the measured bf16 peaks (sustained, burst)",
+        "value": round(shape.T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "launch": "CUDA graph replay of one captured layer call (30 replays)",
+        "layer_tflops": round(lay, 1), "layer_frac_sustained": round(lay / sustained, 4),
+        "layer_frac_burst": round(lay / burst, 4),
+        "gemm1_tflops": round(g1, 1), "gemm1_frac_sustained": round(g1 / sustained, 4),
+        "gemm1_frac_burst": round(g1 / burst, 4),
+        "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        "clocks": clocks,
+    }
 
 
 def _spread(ms):
@@ -635,6 +693,9 @@ def run_ours(args):
         "clocks": clocks,
         "shared_overlap": overlap,
     }
+    if (args.workload == "decode" and not (args.no_prefill or args.experts or args.dtype or args.gated
+                                            or args.shared_fold or args.eager) and world == 1):
+        result["prefill"] = measure_prefill(moe, synth, w, dev, main, peaks)
     if gemm_ab is not None:
         result["gemm_mode_ab"] = gemm_ab
     if option_ab is not None:
