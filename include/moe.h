@@ -144,11 +144,15 @@ typedef enum {
    * gather fused into the grouped GEMM) and x_perm is not written; 0 = the
    * permutation writes x_perm and GEMM-1 reads it. The result is the same. */
   MOE_OPT_GATHER_A = 5,
-  /* Weight rows per MMA of the MX (MXFP8, W4A8) grouped GEMMs: 0 = automatic
-   * (default: 256 for E2M1 weights, 128 for E4M3), 1 = 128
-   * (GEMM-1 gate 64 + up 64; double-buffered accumulators), 2 = 256 (GEMM-1
-   * gate 128 + up 128; GEMM-2 when H % 256 == 0; one accumulator). The result
-   * is the same up to fp32 summation order. */
+  /* Tiling of the MX (MXFP8, W4A8) grouped GEMMs: 0 = automatic (default:
+   * 3 when the GEMM has at most 48 rows per expert on average, as in decode;
+   * otherwise 2 for E2M1 weights and 1 for E4M3), 1 = 128 token rows x 128
+   * weight rows per MMA (GEMM-1 gate 64 + up 64; double-buffered
+   * accumulators), 2 = 128 token rows x 256 weight rows (GEMM-1 gate 128 + up
+   * 128; GEMM-2 when H % 256 == 0; one accumulator), 3 = weights as M: 256
+   * weight rows as two 128-row MMAs against up to 64 token rows of one
+   * expert (GEMM-2 when H % 256 == 0; at most 512 groups; else 2 for E2M1
+   * weights, 1 for E4M3). The result is the same up to fp32 summation order. */
   MOE_OPT_MX_TILE = 6
 } moe_option_t;
 

@@ -323,7 +323,7 @@ MOE_API moe_status_t moe_set_option(moe_handle_t h, moe_option_t opt, int value)
       h->gather_a = value ? 1 : 0;
       return MOE_OK;
     case MOE_OPT_MX_TILE:
-      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 3) return MOE_ERR_INVALID_ARG;
       h->mx_tile = value;
       return MOE_OK;
   }

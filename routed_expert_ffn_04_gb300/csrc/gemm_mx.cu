@@ -470,23 +470,50 @@ cudaError_t gemm_mx_prepare_device() {
       cudaFuncSetAttribute(grouped_gemm_mx_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
-  return gemm_mx_wide_prepare_device();
+  const cudaError_t e = gemm_mx_wide_prepare_device();
+  return e != cudaSuccess ? e : gemm_mx_swap_prepare_device();
+}
+
+// The tiling of an MX GEMM (mode 0: GEMM-1, 1: GEMM-2): 1 = 128 weight rows
+// (this file), 2 = 256 (gemm_mx_wide.cu), 3 = weights as M (gemm_mx_swap.cu).
+// Automatic, by rows per expert as the bf16 GEMMs choose: up to 48 on
+// average (decode) the weights-as-M tiling, whose MMAs carry no token padding
+// (decode shape: MXFP8 GEMM-1 0.358 -> 0.349 ms, 0.99 of HBM); above that 256
+// rows for E2M1 weights, whose 128-row kernels are bound by their MMA issue
+// rate (W4A8 GEMM-1 0.64 -> 0.77 of HBM, GEMM-2 0.238 -> 0.203 ms), and 128
+// rows for E4M3 weights, which stream at the HBM rate either way.
+int pick_mx_tile(const GroupedGemmArgs& a, int mode) {
+  int t = a.mx_tile;
+  if (t == 0) {
+    const int G = a.offsets ? a.G : 1;
+    const double avg_rows = (double)a.rows / (G > 0 ? G : 1);
+    t = avg_rows <= 48.0 ? 3 : (a.w4 ? 2 : 1);
+  }
+  if (t == 3 && !gemm_mx_swap_supported(a, mode)) t = a.w4 ? 2 : 1;
+  if (t == 2 && !gemm_mx_wide_supported(a, mode)) t = 1;
+  return t;
 }
 
 cudaError_t launch_gemm_mx_gate_up(const GroupedGemmArgs& a, cudaStream_t s) {
-  // Automatic: the 256-row tile for E2M1 weights, whose 128-row GEMM-1 is
-  // bound by its MMA issue rate; E4M3 weights stream at the HBM rate either way.
-  if ((a.mx_tile == 2 || (a.mx_tile == 0 && a.w4)) && gemm_mx_wide_supported(a, 0))
-    return launch_gemm_mx_wide_gate_up(a, s);
-  return a.w4 ? run_gemm_mx<0, true>(a, s) : run_gemm_mx<0, false>(a, s);
+  switch (pick_mx_tile(a, 0)) {
+    case 3:
+      return launch_gemm_mx_swap_gate_up(a, s);
+    case 2:
+      return launch_gemm_mx_wide_gate_up(a, s);
+    default:
+      return a.w4 ? run_gemm_mx<0, true>(a, s) : run_gemm_mx<0, false>(a, s);
+  }
 }
 
 cudaError_t launch_gemm_mx_down(const GroupedGemmArgs& a, cudaStream_t s) {
-  // Automatic: the 256-row tile for E2M1 weights, as for GEMM-1 (W4A8 GEMM-2
-  // 0.238 -> 0.203 ms); for E4M3 it measured within 2% either way.
-  if ((a.mx_tile == 2 || (a.mx_tile == 0 && a.w4)) && gemm_mx_wide_supported(a, 1))
-    return launch_gemm_mx_wide_down(a, s);
-  return a.w4 ? run_gemm_mx<1, true>(a, s) : run_gemm_mx<1, false>(a, s);
+  switch (pick_mx_tile(a, 1)) {
+    case 3:
+      return launch_gemm_mx_swap_down(a, s);
+    case 2:
+      return launch_gemm_mx_wide_down(a, s);
+    default:
+      return a.w4 ? run_gemm_mx<1, true>(a, s) : run_gemm_mx<1, false>(a, s);
+  }
 }
 
 }  // namespace moe

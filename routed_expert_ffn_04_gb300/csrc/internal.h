@@ -93,8 +93,8 @@ struct GroupedGemmArgs {
   const uint8_t* s_gate;
   const uint8_t* s_down;
   int w4;
-  // MX GEMM-1 weight tile: 0 auto, 1 = 128 rows (gemm_mx.cu), 2 = 256 rows
-  // (gemm_mx_wide.cu).
+  // MX GEMM tiling: 0 auto, 1 = 128 weight rows (gemm_mx.cu), 2 = 256 rows
+  // (gemm_mx_wide.cu), 3 = weights as M (gemm_mx_swap.cu).
   int mx_tile;
   // bf16 GEMM-1, tokens-as-M tiling: gather the A rows from x instead of
   // reading a: row r is token gather_src[r] / gather_k of gather_x [T, H]
@@ -141,6 +141,12 @@ bool gemm_mx_wide_supported(const GroupedGemmArgs& a, int mode);
 cudaError_t gemm_mx_wide_prepare_device();
 cudaError_t launch_gemm_mx_wide_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_mx_wide_down(const GroupedGemmArgs& a, cudaStream_t s);
+// MX GEMMs with the weights as M (gemm_mx_swap.cu): 256 weight rows against
+// up to 64 token rows per tile; up to 512 groups; GEMM-2 needs H % 256 == 0.
+bool gemm_mx_swap_supported(const GroupedGemmArgs& a, int mode);
+cudaError_t gemm_mx_swap_prepare_device();
+cudaError_t launch_gemm_mx_swap_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_mx_swap_down(const GroupedGemmArgs& a, cudaStream_t s);
 // The tiling launch_gemm_gate_up / launch_gemm_down will use (GemmMode).
 int gemm_pick_mode(const GroupedGemmArgs& a);
 cudaError_t launch_gemm_gate_up(const GroupedGemmArgs& a, cudaStream_t s);
