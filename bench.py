@@ -47,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM1_TRAFFIC = {
     "decode": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1212235264 + 3315200) / 1213726720),      # E = 48
     "prefill": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1164402432 + 191267840) / 1073741824),  # E = 32, A gathered
-    "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "02a418cdc801d075", (692628992 + 24681472) / 718012416),       # E = 48
+    "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "17f506ddc941a0af", (692628992 + 24681472) / 718012416),       # E = 48 (since: tiling dispatch only)
     "mxfp4": (('gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "fb1710b0057f2698", (390629632 + 21867008) / 416022528),  # E = 48, 256-row tile
 }
 
