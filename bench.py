@@ -49,6 +49,9 @@ GEMM1_TRAFFIC = {
     "prefill": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1164402432 + 191267840) / 1073741824),  # E = 32, A gathered
     "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "17f506ddc941a0af", (692628992 + 24681472) / 718012416),       # E = 48 (since: tiling dispatch only)
     "mxfp4": (('gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "fb1710b0057f2698", (390629632 + 21867008) / 416022528),  # E = 48, 256-row tile
+    # the decode shape with MX operands (--dtype): the weights-as-M GEMM-1
+    "decode:mxfp8": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "e0200ff648a31c45", (625858560 + 3338496) / 625827840),   # E = 48
+    "decode:mxfp4": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "e0200ff648a31c45", (323884800 + 2910720) / 323837952),   # E = 48
 }
 
 
@@ -624,10 +627,11 @@ def run_ours(args):
             peak_src += " x 2 (fp8 / bf16 nominal ratio)"
         unit = "TFLOP/s"
     traffic = None
-    if (args.workload in GEMM1_TRAFFIC and not args.experts and not args.dtype and not args.gated
+    tkey = f"{args.workload}:{args.dtype}" if args.dtype else args.workload
+    if (tkey in GEMM1_TRAFFIC and not args.experts and not args.gated
             and not args.shared_fold and args.gemm_mode == 0
-            and source_sha(GEMM1_TRAFFIC[args.workload][0]) == GEMM1_TRAFFIC[args.workload][1]):
-        traffic = int(round(GEMM1_TRAFFIC[args.workload][2] * work["gemm1_bytes"]))
+            and source_sha(GEMM1_TRAFFIC[tkey][0]) == GEMM1_TRAFFIC[tkey][1]):
+        traffic = int(round(GEMM1_TRAFFIC[tkey][2] * work["gemm1_bytes"]))
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
     layer_tflops = work["flops"] / (ms * 1e-3) / 1e12
     # route 1; permute 1 (one block up to 16384 pairs, else 3) + row gather 1;
