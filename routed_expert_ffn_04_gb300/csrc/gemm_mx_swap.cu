@@ -79,7 +79,9 @@ constexpr int sSfCol0 = 2 * sAccCols;      // TMEM scale slot s: sSfCol0 + 16 s
 constexpr int sTmemCols = 512;
 constexpr int sMaxGroups = 512;
 constexpr int sTableStride = sMaxGroups + 8;
-constexpr int sTableBytes = 3 * sTableStride * 4;  // tile starts, row starts, atom-block starts
+constexpr int sTileList = 64;              // a CTA's first tiles, decoded once in the prologue
+constexpr int sTableBytes = 3 * sTableStride * 4 + sTileList * (int)sizeof(TileInfo);  // tile starts, row
+                                           // starts, atom-block starts, the CTA's tile list
 constexpr int sXchBlock = 32 * 32;         // fp32 values one up warp hands over per chunk
 constexpr int sXchBytes = 4 * sXchBlock * 4;  // one block per gate/up quarter pair of each half
 constexpr int sNumBars = 2 * sStages + 2 * sGroupSlots + 4 + 2 + 8;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(sThreads, 1)
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + sOffTable);
   int32_t* row_start = tile_start + sTableStride;
   int32_t* blk_start = row_start + sTableStride;
+  TileInfo* tlist = reinterpret_cast<TileInfo*>(blk_start + sTableStride);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + sOffBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + sNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -270,6 +273,18 @@ __global__ void __launch_bounds__(sThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = tile_start[p.G];
   const int n_k = p.num_kb / 2;  // p.num_kb counts 64-wide slices; a stage holds two
+  // The CTA's k-th tile (blockIdx.x + k * gridDim.x), decoded once here for the
+  // first sTileList: a role starting a tile then reads it from shared memory
+  // instead of searching the group table (a tile boundary cost the MMA thread
+  // about a stage's time, the weight producer three).
+  for (int k = threadIdx.x; k < sTileList; k += sThreads) {
+    const int tile = blockIdx.x + k * (int)gridDim.x;
+    if (tile < total) tlist[k] = decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+  }
+  __syncthreads();
+  auto tile_info = [&](int k, int tile) -> TileInfo {
+    return k < sTileList ? tlist[k] : decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer
@@ -279,9 +294,9 @@ __global__ void __launch_bounds__(sThreads, 1)
       Armed armed, armed_g;
       bool ok = true;
       // Atom groups: a group is up to sGroup consecutive K stages of one tile.
-      int g_tile = blockIdx.x, g_kb = 0, nload = 0;
+      int g_tile = blockIdx.x, g_k = 0, g_kb = 0, nload = 0;
       TileInfo g_ti{};
-      if (g_tile < total) g_ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, g_tile);
+      if (g_tile < total) g_ti = tile_info(0, g_tile);
       auto load_group = [&]() -> bool {
         if (g_tile >= total) return true;
         const int gs = nload % sGroupSlots;
@@ -313,7 +328,8 @@ __global__ void __launch_bounds__(sThreads, 1)
         if (g_kb == n_k) {
           g_kb = 0;
           g_tile += gridDim.x;
-          if (g_tile < total) g_ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, g_tile);
+          ++g_k;
+          if (g_tile < total) g_ti = tile_info(g_k, g_tile);
         }
         return true;
       };
@@ -333,15 +349,15 @@ __global__ void __launch_bounds__(sThreads, 1)
       };
       for (int i = 0; ok && i < sGroupAhead; ++i) ok = load_group();
       int j = 0;  // stage
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+      for (int tile = blockIdx.x, k = 0; ok && tile < total; tile += gridDim.x, ++k) {
+        const TileInfo ti = tile_info(k, tile);
         const int w_row = ti.g * p.N + ti.wt * kCols;
         // Tile order: GEMM-1 the gate/up pair block t (256 rows), GEMM-2 the
         // 128-row down blocks t and t + 1.
         const int t = block_of(ti);
         const bool has_next = tile + (int)gridDim.x < total;
         const int t_next =
-            has_next ? block_of(decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile + gridDim.x)) : 0;
+            has_next ? block_of(tile_info(k + 1, tile + gridDim.x)) : 0;
         const int rem = ti.nrows - ti.tt * sTokRows;
         const int nb = ((rem < sTokRows ? rem : sTokRows) + sTokBox - 1) / sTokBox;
         const uint32_t tx = kTxW + (uint32_t)nb * kTxBox;
@@ -401,8 +417,8 @@ __global__ void __launch_bounds__(sThreads, 1)
       bool ok = true;
       Armed armed;
       int j = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+      for (int tile = blockIdx.x, k = 0; ok && tile < total; tile += gridDim.x, ++k) {
+        const TileInfo ti = tile_info(k, tile);
         const int row = ti.row0 + ti.tt * sTokRows;
         const int rem = ti.nrows - ti.tt * sTokRows;
         const int nb = ((rem < sTokRows ? rem : sTokRows) + sTokBox - 1) / sTokBox;
@@ -481,7 +497,7 @@ __global__ void __launch_bounds__(sThreads, 1)
           break;
         }
         tc_fence_after();
-        const TileInfo ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+        const TileInfo ti = tile_info(local, tile);
         const uint32_t d = tmem_base + (uint32_t)(acc * sAccCols);
         const uint32_t sfb_col = 2u * (uint32_t)(ti.tt & 1);  // odd chunks: rows 64-127 of the token atom
         for (int kb = 0; kb < n_k; ++kb, ++j) {
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(sThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const TileInfo ti = decode_tile_s<sTokRows>(p.G, tile_start, row_start, tile);
+      const TileInfo ti = tile_info(local, tile);
       const int r_first = ti.tt * sTokRows;  // first token row of the chunk within its group
       const int rem = ti.nrows - r_first;
       const int ncols = rem < sTokRows ? rem : sTokRows;
@@ -563,13 +579,14 @@ __global__ void __launch_bounds__(sThreads, 1)
             if (e > 0 && !warp_wait(xfree(xi), (uint32_t)(e - 1) & 1u, abort_flag, p.status, p.limit_ns))
               return false;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) xb[jj * 32 + lane] = __uint_as_float(v[jj]);
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj < n) xb[jj * 32 + lane] = __uint_as_float(v[jj]);
             mbar_arrive(xfull(xi));
           } else {
             if (!warp_wait(xfull(xi), (uint32_t)e & 1u, abort_flag, p.status, p.limit_ns)) return false;
             float u[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) u[jj] = xb[jj * 32 + lane];
+            for (int jj = 0; jj < 32; ++jj) u[jj] = jj < n ? xb[jj * 32 + lane] : 0.0f;
             mbar_arrive(xfree(xi));
             store_h_tokens(v, u, n, h_col + (size_t)(32 * c) * p.N, p.N, r_first + 32 * c, lane, scale_blk0,
                            p.N / 128, jcol);
