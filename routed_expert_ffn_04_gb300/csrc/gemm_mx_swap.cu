@@ -30,7 +30,9 @@
 // The pipeline is that of gemm_mx_wide.cu (one barrier per stage for the MMA
 // thread, the weight ring, the token ring and the TMEM scale slot freed by one
 // commit; scale atoms two stages per bulk copy, two groups ahead), with two
-// accumulators so that a tile's MMAs do not wait for the previous epilogue.
+// accumulators so that a tile's MMAs do not wait for the previous epilogue,
+// and each CTA's first 64 tiles decoded once into shared memory, so that no
+// role searches the group table at a tile boundary.
 //
 // Persistent, one CTA per SM, 384 threads:
 //   warp 0      weight producer: per 128-wide K stage the tile's 256 weight

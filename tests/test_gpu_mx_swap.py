@@ -177,3 +177,22 @@ def test_swap_layer_decode_shape_tile_edges(handle, dtype):
     ref = oracle.layer_forward_mx(x.cpu(), logits.cpu(), _w_oracle(w, w4), K=shape.K, scaling=shape.scaling,
                                   tokens=tokens, w4=w4)
     _check(out.float().cpu().numpy()[tokens], ref, f"decode shape {dtype}, weights as M")
+
+
+def test_more_tiles_per_cta_than_the_prologue_list(handle):
+    # A CTA decodes its first 64 tiles once in the prologue and searches the
+    # group table for the rest. 64 groups of 320 rows (five 64-row chunks) x 32
+    # weight tiles of I = 4096 give 10240 GEMM-1 tiles, about 67 per CTA on 152
+    # SMs; the last groups' tiles are the ones past the list.
+    H, I, G = 256, 4096, 64
+    sizes = [320] * G
+    G, offsets, a, wg, wu, wd = _operands(H, I, sizes, 35)
+    aq, as_ = moe.quantize_mx(handle, a.cuda())
+    pw = _quantised_weights(handle, wg, wu, wd, False)
+    y = _run_gemm(handle, SWAP, aq, as_, offsets, pw, H, I, G, moe.MOE_MXFP8_E4M3)
+    xq, xs = oracle.mx_quantize(a)
+    q = oracle.mx_quantize
+    for gi in (0, G - 2, G - 1):
+        r0, r1 = offsets[gi], offsets[gi + 1]
+        ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], q(wg[gi]), q(wu[gi]), q(wd[gi]))
+        _check(y[r0:r1], ref, f"group {gi}")
