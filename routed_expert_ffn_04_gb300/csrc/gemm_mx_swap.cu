@@ -34,7 +34,7 @@
 // and each CTA's first 64 tiles decoded once into shared memory, so that no
 // role searches the group table at a tile boundary.
 //
-// Persistent, one CTA per SM, 384 threads:
+// Persistent, one CTA per SM, 416 threads:
 //   warp 0      weight producer: per 128-wide K stage the tile's 256 weight
 //               rows (one box for E2M1 in tile order, four for row-major
 //               E4M3), 4-stage ring; the scale atoms of stage pairs; for
@@ -42,7 +42,8 @@
 //   warp 11     token producer: the chunk's rows in 16-row boxes, completing
 //               on the weight stage's barrier.
 //   warp 2      scale warp: three tcgen05.cp per stage into the stage's slot.
-//   warp 1      TMEM allocator + MMA issuer: 8 MMAs (two halves x K = 32).
+//   warps 1, 12 MMA issuers (warp 1 also allocates TMEM): 4 MMAs (K = 32)
+//               each per stage, one per accumulator half.
 //   warps 3-10  epilogue: warp w reads TMEM lane quarter w % 4 of accumulator
 //               half (w - 3) / 4.
 // TMEM: two accumulators of 2 x 64 columns, then one 16-column scale slot per
@@ -64,11 +65,12 @@ constexpr int sStages = 4;                 // weight ring = token ring = TMEM sc
 constexpr int sGroup = 2;                  // K stages per atom group (one bulk copy per atom kind)
 constexpr int sGroupSlots = 4;             // atom groups in shared memory
 constexpr int sGroupAhead = 2;             // groups between an atom group's load and its first stage
-constexpr int sThreads = 384;
+constexpr int sThreads = 416;
 constexpr int sScaleWarp = 2;
 constexpr int sEpiWarp0 = 3;
 constexpr int sEpiWarps = 8;
 constexpr int sProdTWarp = 11;
+constexpr int sMmaWarp2 = 12;             // issues accumulator half 1's MMAs (warp 1 half 0's)
 constexpr int sPrefetch = 4;               // E2M1 GEMM-1: L2 prefetch this many stages ahead of the ring
 constexpr int sTokRows = 64;               // token rows per tile = MMA N
 constexpr int sTokBox = 16;                // token rows per TMA box
@@ -86,7 +88,7 @@ constexpr int sTableBytes = 3 * sTableStride * 4 + sTileList * (int)sizeof(TileI
                                            // starts, atom-block starts, the CTA's tile list
 constexpr int sXchBlock = 32 * 32;         // fp32 values one up warp hands over per chunk
 constexpr int sXchBytes = 4 * sXchBlock * 4;  // one block per gate/up quarter pair of each half
-constexpr int sNumBars = 2 * sStages + 2 * sGroupSlots + 4 + 2 + 8;
+constexpr int sNumBars = 2 * sStages + 2 * sGroupSlots + 4 + 2 + 8 + 1;
 constexpr int sBarBytes = 512;
 // Shared memory: weight ring | token ring | atom groups | exchange | tables | barriers.
 constexpr int sOffT = sStages * sWTile;
@@ -101,7 +103,8 @@ static_assert(sNumBars * 8 + 8 <= sBarBytes, "barrier area");
 static_assert(sTTile % 1024 == 0 && (sTokBox * 128) % 1024 == 0, "1024-byte alignment of swizzled token boxes");
 static_assert(sOffXch % 16 == 0 && sOffTable % 16 == 0 && sOffBars % 8 == 0, "alignment");
 static_assert(sTokRows % sTokBox == 0 && sTokRows == 64, "a chunk is half an activation atom");
-static_assert(sThreads == 32 * (sProdTWarp + 1) && sEpiWarp0 + sEpiWarps == sProdTWarp, "warp roles");
+static_assert(sThreads == 32 * (sMmaWarp2 + 1) && sProdTWarp + 1 == sMmaWarp2 && sEpiWarp0 + sEpiWarps == sProdTWarp,
+              "warp roles");
 
 // Parity of the phase of a ring barrier that completes for the n-th time
 // (n = 0, 1, ...) when stage n * depth + slot completes.
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(sThreads, 1)
   // when the up warp wrote a chunk, xfree when the gate warp read it.
   auto xfull = [&](int x) { return tbar0 + 48u + 8u * x; };
   auto xfree = [&](int x) { return tbar0 + 80u + 8u * x; };
+  const uint32_t drain_bar2 = tbar0 + 112u;  // the second MMA thread's drain
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = p.N / kCols;
@@ -238,17 +242,18 @@ __global__ void __launch_bounds__(sThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < sStages; ++s) {
       mbar_init(full(s), 2);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), 2);  // one commit from each MMA thread
     }
     for (int g = 0; g < sGroupSlots; ++g) {
       mbar_init(gfull(g), 1);
       mbar_init(gfree(g), 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull(a), 1);
+      mbar_init(tfull(a), 2);
       mbar_init(tempty(a), sEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(drain_bar2, 1);
     mbar_init(sdrain_bar, 1);
     for (int x = 0; x < 4; ++x) {
       mbar_init(xfull(x), 32);
@@ -486,9 +491,14 @@ __global__ void __launch_bounds__(sThreads, 1)
         drain_wait(sdrain_bar, 0, 100000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == sMmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues accumulator half 0's MMAs, warp sMmaWarp2 half 1's: each
+    // tcgen05.mma costs its issuing thread ~55 cycles, 8 a stage were most of
+    // one thread's stage time. Each commits to empty(s) and tfull (count 2).
     if (lane == 0) {
+      const int hsel = warp == 1 ? 0 : 1;
+      const uint32_t drain = hsel ? drain_bar2 : drain_bar;
       bool ok = true, issued = false;
       int local = 0, j = 0;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
@@ -500,7 +510,7 @@ __global__ void __launch_bounds__(sThreads, 1)
         }
         tc_fence_after();
         const TileInfo ti = tile_info(local, tile);
-        const uint32_t d = tmem_base + (uint32_t)(acc * sAccCols);
+        const uint32_t d = tmem_base + (uint32_t)(acc * sAccCols + hsel * sTokRows);
         const uint32_t sfb_col = 2u * (uint32_t)(ti.tt & 1);  // odd chunks: rows 64-127 of the token atom
         for (int kb = 0; kb < n_k; ++kb, ++j) {
           const int s = j % sStages;
@@ -512,16 +522,14 @@ __global__ void __launch_bounds__(sThreads, 1)
           tc_fence_after();
           // +32 bytes along K is +2 in a descriptor's start-address field.
           const uint64_t dt = sw128_kmajor_desc(sm0 + sOffT + s * sTTile);
-          const uint64_t dw0 = sw128_kmajor_desc(sm0 + s * sWTile);
-          const uint64_t dw1 = sw128_kmajor_desc(sm0 + s * sWTile + 128 * 128);
+          const uint64_t dw = sw128_kmajor_desc(sm0 + s * sWTile + hsel * (128 * 128));  // weight rows 128 hsel..
           const uint32_t sf = tmem_base + (uint32_t)(sSfCol0 + 16 * s);
+          const uint32_t sfa = sf + 8 + 4 * hsel;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             // Scale ids (bits 4-5 for B, 29-30 for A) pick byte k of the scale words.
             const uint32_t id = kIdesc0 | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-            const uint32_t accum = (kb | k) ? 1u : 0u;
-            umma_mxf8(d, dw0 + 2 * k, dt + 2 * k, id, sf + 8, sf + sfb_col, accum);
-            umma_mxf8(d + sTokRows, dw1 + 2 * k, dt + 2 * k, id, sf + 12, sf + sfb_col, accum);
+            umma_mxf8(d, dw + 2 * k, dt + 2 * k, id, sfa, sf + sfb_col, (kb | k) ? 1u : 0u);
           }
           issued = true;
           umma_commit(empty(s));
@@ -530,8 +538,8 @@ __global__ void __launch_bounds__(sThreads, 1)
         umma_commit(tfull(acc));
       }
       if (!ok && issued) {
-        umma_commit(drain_bar);
-        drain_wait(drain_bar, 0, 100000000ull);
+        umma_commit(drain);
+        drain_wait(drain, 0, 100000000ull);
       }
     }
   } else {
