@@ -27,10 +27,11 @@
 // finds the scale of B column n in column n / 32 of its scale address, so an
 // odd chunk points the B scale address two columns into the atom.
 //
-// The pipeline is that of gemm_mx_wide.cu (one barrier per stage for the MMA
-// thread, the weight ring, the token ring and the TMEM scale slot freed by one
-// commit; scale atoms two stages per bulk copy, two groups ahead), with two
-// accumulators so that a tile's MMAs do not wait for the previous epilogue,
+// The pipeline is that of gemm_mx_wide.cu (one barrier wait per stage for an
+// MMA thread, the weight ring, the token ring and the TMEM scale slot freed
+// together by the MMA threads' commits; scale atoms two stages per bulk copy,
+// two groups ahead), with two accumulators so that a tile's MMAs do not wait
+// for the previous epilogue,
 // and each CTA's first 64 tiles decoded once into shared memory, so that no
 // role searches the group table at a tile boundary.
 //
