@@ -50,8 +50,8 @@ GEMM1_TRAFFIC = {
     "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "17f506ddc941a0af", (692628992 + 24681472) / 718012416),       # E = 48 (since: tiling dispatch only)
     "mxfp4": (('gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "fb1710b0057f2698", (390629632 + 21867008) / 416022528),  # E = 48, 256-row tile
     # the decode shape with MX operands (--dtype): the weights-as-M GEMM-1
-    "decode:mxfp8": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "e0200ff648a31c45", (625858560 + 3338496) / 625827840),   # E = 48
-    "decode:mxfp4": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "e0200ff648a31c45", (323884800 + 2910720) / 323837952),   # E = 48
+    "decode:mxfp8": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "76992db8f54232a1", (625859072 + 3213056) / 625827840),   # E = 48
+    "decode:mxfp4": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "76992db8f54232a1", (323884032 + 2906112) / 323837952),   # E = 48
 }
 
 
