@@ -123,9 +123,10 @@ def test_pack_mx_scales_bit_exact(handle, rows, cols):
     assert np.array_equal(pair, want.reshape(2 * rows, cols // 32))
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+# MOE_OPT_MX_TILE: 0 automatic, 1 the 128-row tile, 2 the 256-row tile, 3 weights as M.
+@pytest.mark.parametrize("tile", [0, 1, 2, 3])
 @pytest.mark.parametrize("H,I,sizes", [(256, 128, [16, 0, 3, 1]), (512, 384, [0, 1, 37, 130, 300, 0])])
-def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
+def test_mx_grouped_gemm_matches_oracle(handle, tile, H, I, sizes):
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     rows = int(offsets[-1])
@@ -135,14 +136,17 @@ def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
     aq, as_ = moe.quantize_mx(handle, a.cuda())
     mw = moe.quantize_weights_mx(handle, {"w_gate": wg.cuda(), "w_up": wu.cuda(), "w_down": wd.cuda()})
     pw = moe.pack_weights_mx(handle, mw)
-    handle.set_option(moe.MOE_OPT_GEMM_MODE, mode)
+    handle.set_option(moe.MOE_OPT_MX_TILE, tile)
     y = torch.full((rows, H), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I, moe.MOE_MXFP8_E4M3, num_groups=G), dtype=torch.uint8,
                      device="cuda")
-    moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), pw["w_gate"], pw["w_up"], pw["w_down"], y, ws,
-                            num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP8_E4M3, a_scale=as_, s_gate=pw["s_gate"],
-                            s_down=pw["s_down"])
-    torch.cuda.synchronize()
+    try:
+        moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), pw["w_gate"], pw["w_up"], pw["w_down"],
+                                y, ws, num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP8_E4M3, a_scale=as_,
+                                s_gate=pw["s_gate"], s_down=pw["s_down"])
+        torch.cuda.synchronize()
+    finally:
+        handle.set_option(moe.MOE_OPT_MX_TILE, 0)
     assert handle.device_status() == 0
     yh = y.cpu().numpy()
     xq, xs = oracle.mx_quantize(a)
@@ -152,7 +156,7 @@ def test_mx_grouped_gemm_matches_oracle(handle, mode, H, I, sizes):
             continue
         ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], oracle.mx_quantize(wg[gi]), oracle.mx_quantize(wu[gi]),
                                    oracle.mx_quantize(wd[gi]))
-        _check(yh[r0:r1], ref, f"group {gi} mode {mode}")
+        _check(yh[r0:r1], ref, f"group {gi} tile {tile}")
     assert np.all(np.isnan(yh[offsets[-1]:]))
 
 

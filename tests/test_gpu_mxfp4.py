@@ -85,8 +85,10 @@ def _w4a8_weights_oracle(w):
             for k, v in w.items()}
 
 
+# MOE_OPT_MX_TILE: 0 automatic, 1 the 128-row tile, 2 the 256-row tile, 3 weights as M.
+@pytest.mark.parametrize("tile", [0, 1, 2, 3])
 @pytest.mark.parametrize("H,I,sizes", [(256, 128, [16, 0, 3, 1]), (512, 384, [0, 1, 37, 130, 300, 0])])
-def test_w4a8_grouped_gemm_matches_oracle(handle, H, I, sizes):
+def test_w4a8_grouped_gemm_matches_oracle(handle, tile, H, I, sizes):
     G = len(sizes)
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     rows = int(offsets[-1])
@@ -100,10 +102,14 @@ def test_w4a8_grouped_gemm_matches_oracle(handle, H, I, sizes):
     y = torch.full((rows, H), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(moe.grouped_gemm_workspace_size(rows, H, I, moe.MOE_MXFP4_W4A8, num_groups=G), dtype=torch.uint8,
                      device="cuda")
-    moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), pw["w_gate"], pw["w_up"], pw["w_down"], y, ws,
-                            num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP4_W4A8, a_scale=as_, s_gate=pw["s_gate"],
-                            s_down=pw["s_down"])
-    torch.cuda.synchronize()
+    handle.set_option(moe.MOE_OPT_MX_TILE, tile)
+    try:
+        moe.grouped_swiglu_gemm(handle, aq, torch.from_numpy(offsets).cuda(), pw["w_gate"], pw["w_up"], pw["w_down"],
+                                y, ws, num_groups=G, H=H, I=I, dtype=moe.MOE_MXFP4_W4A8, a_scale=as_,
+                                s_gate=pw["s_gate"], s_down=pw["s_down"])
+        torch.cuda.synchronize()
+    finally:
+        handle.set_option(moe.MOE_OPT_MX_TILE, 0)
     assert handle.device_status() == 0
     yh = y.cpu().numpy()
     xq, xs = oracle.mx_quantize(a)
@@ -113,7 +119,7 @@ def test_w4a8_grouped_gemm_matches_oracle(handle, H, I, sizes):
             continue
         ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], oracle.mxfp4_quantize(wg[gi]), oracle.mxfp4_quantize(wu[gi]),
                                    oracle.mxfp4_quantize(wd[gi]), w4=True)
-        _check(yh[r0:r1], ref, f"group {gi}")
+        _check(yh[r0:r1], ref, f"group {gi} tile {tile}")
     assert np.all(np.isnan(yh[offsets[-1]:]))
 
 
