@@ -79,6 +79,8 @@ def parse():
                     help="skip the shared-expert overlap measurement (shorter runs, e.g. under a profiler)")
     ap.add_argument("--gemm-mode", type=int, default=0,
                     help="MOE_OPT_GEMM_MODE for the timed calls (0 automatic, 1 weights-as-M, 2 tokens-as-M, 3 CTA pair)")
+    ap.add_argument("--mx-tile", type=int, default=0,
+                    help="MOE_OPT_MX_TILE for the timed calls (0 automatic, 1 128-row, 2 256-row, 3 weights as M)")
     ap.add_argument("--ab-gemm-modes", default="",
                     help="comma-separated GEMM modes to time against each other (interleaved graph replays)")
     ap.add_argument("--ab-option", default="",
@@ -506,6 +508,7 @@ def run_ours(args):
     w = synth.make_weights(shape, device=dev, seed=0)
     layer = moe.MoELayer(shape, w, device=local)
     layer.handle.set_option(moe.MOE_OPT_GEMM_MODE, args.gemm_mode)
+    layer.handle.set_option(moe.MOE_OPT_MX_TILE, args.mx_tile)
     if args.shared_fold:
         layer.handle.set_option(moe.MOE_OPT_SHARED_FOLD, 1)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
@@ -629,7 +632,7 @@ def run_ours(args):
     traffic = None
     tkey = f"{args.workload}:{args.dtype}" if args.dtype else args.workload
     if (tkey in GEMM1_TRAFFIC and not args.experts and not args.gated
-            and not args.shared_fold and args.gemm_mode == 0
+            and not args.shared_fold and args.gemm_mode == 0 and args.mx_tile == 0
             and source_sha(GEMM1_TRAFFIC[tkey][0]) == GEMM1_TRAFFIC[tkey][1]):
         traffic = int(round(GEMM1_TRAFFIC[tkey][2] * work["gemm1_bytes"]))
     layer_gbs = work["layer_bytes"] / (ms * 1e-3) / 1e9
@@ -674,6 +677,7 @@ def run_ours(args):
                               else "given fp32 logits"),
             "shared_expert": ("one more group of the routed GEMMs" if args.shared_fold and shape.dtype == "bf16"
                               and shape.I_shared == shape.I else "side stream, event-ordered"),
+            **({"mx_tile": args.mx_tile} if args.mx_tile else {}),
         },
         "roofline": {
             "kernel": "routed grouped GEMM-1 (gate/up + SwiGLU)",
