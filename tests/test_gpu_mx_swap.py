@@ -196,3 +196,18 @@ def test_more_tiles_per_cta_than_the_prologue_list(handle):
         r0, r1 = offsets[gi], offsets[gi + 1]
         ref = oracle.swiglu_mlp_mx(xq[r0:r1], xs[r0:r1], q(wg[gi]), q(wu[gi]), q(wd[gi]))
         _check(y[r0:r1], ref, f"group {gi}")
+
+
+@pytest.mark.parametrize("G,fallback", [(512, False), (513, True)])
+def test_group_table_limit(handle, G, fallback):
+    # The weights-as-M kernels hold up to 512 groups in shared memory: 512 run
+    # them, 513 take the 128-row kernels (E4M3 weights), same results either way.
+    H, I = 256, 128
+    sizes = [0] * G
+    for gi, n in ((0, 3), (100, 1), (257, 70), (G - 2, 5), (G - 1, 33)):
+        sizes[gi] = n
+    G, offsets, a, wg, wu, wd = _operands(H, I, sizes, 36)
+    aq, as_ = moe.quantize_mx(handle, a.cuda())
+    pw = _quantised_weights(handle, wg, wu, wd, False)
+    y = _run_gemm(handle, SWAP, aq, as_, offsets, pw, H, I, G, moe.MOE_MXFP8_E4M3)
+    _per_group(y, offsets, a, wg, wu, wd, False)
