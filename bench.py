@@ -47,8 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM1_TRAFFIC = {
     "decode": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1212235264 + 3315200) / 1213726720),      # E = 48
     "prefill": (('gemm.cu', 'gemm_sched.cuh', 'ptx.cuh'), "5a8519b54d77f16e", (1164402432 + 191267840) / 1073741824),  # E = 32, A gathered
-    "mxfp8": (('gemm_mx.cu', 'gemm_sched.cuh', 'ptx.cuh'), "17f506ddc941a0af", (692628992 + 24681472) / 718012416),       # E = 48 (since: tiling dispatch only)
-    "mxfp4": (('gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "fb1710b0057f2698", (390629632 + 21867008) / 416022528),  # E = 48, 256-row tile
+    "mxfp8": (('gemm_mx.cu', 'gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "681f1db6bab86a2c", (693172736 + 23758848) / 718012416),  # E = 48, 256-row tile
+    "mxfp4": (('gemm_mx.cu', 'gemm_mx_wide.cu', 'gemm_sched.cuh', 'ptx.cuh'), "681f1db6bab86a2c", (390695168 + 22090496) / 416022528),  # E = 48, 256-row tile
     # the decode shape with MX operands (--dtype): the weights-as-M GEMM-1
     "decode:mxfp8": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "76992db8f54232a1", (625859072 + 3213056) / 625827840),   # E = 48
     "decode:mxfp4": (('gemm_mx_swap.cu', 'gemm_sched.cuh', 'ptx.cuh'), "76992db8f54232a1", (323884032 + 2906112) / 323837952),   # E = 48

@@ -146,7 +146,8 @@ typedef enum {
   MOE_OPT_GATHER_A = 5,
   /* Tiling of the MX (MXFP8, W4A8) grouped GEMMs: 0 = automatic (default:
    * 3 when the GEMM has at most 48 rows per expert on average, as in decode;
-   * otherwise 2 for E2M1 weights and 1 for E4M3), 1 = 128 token rows x 128
+   * otherwise 2, except 1 for a single group with E4M3 weights such as the
+   * shared expert), 1 = 128 token rows x 128
    * weight rows per MMA (GEMM-1 gate 64 + up 64; double-buffered
    * accumulators), 2 = 128 token rows x 256 weight rows (GEMM-1 gate 128 + up
    * 128; GEMM-2 when H % 256 == 0; one accumulator), 3 = weights as M: 256

@@ -479,15 +479,16 @@ cudaError_t gemm_mx_prepare_device() {
 // Automatic, by rows per expert as the bf16 GEMMs choose: up to 48 on
 // average (decode) the weights-as-M tiling, whose MMAs carry no token padding
 // (decode shape: MXFP8 GEMM-1 0.358 -> 0.349 ms, 0.99 of HBM); above that 256
-// rows for E2M1 weights, whose 128-row kernels are bound by their MMA issue
-// rate (W4A8 GEMM-1 0.64 -> 0.77 of HBM, GEMM-2 0.238 -> 0.203 ms), and 128
-// rows for E4M3 weights, which stream at the HBM rate either way.
+// rows for the routed experts (T = 2048: W4A8 GEMM-1 0.64 -> 0.77 of HBM;
+// MXFP8 GEMM-1 0.410 -> 0.403 ms, GEMM-2 0.240 -> 0.226 ms), and 128 rows for
+// a single group with E4M3 weights (the shared expert), whose 256-row tiles
+// would be half as many and leave SMs idle.
 int pick_mx_tile(const GroupedGemmArgs& a, int mode) {
   int t = a.mx_tile;
   if (t == 0) {
     const int G = a.offsets ? a.G : 1;
     const double avg_rows = (double)a.rows / (G > 0 ? G : 1);
-    t = avg_rows <= 48.0 ? 3 : (a.w4 ? 2 : 1);
+    t = avg_rows <= 48.0 ? 3 : ((a.w4 || G > 1) ? 2 : 1);
   }
   if (t == 3 && !gemm_mx_swap_supported(a, mode)) t = a.w4 ? 2 : 1;
   if (t == 2 && !gemm_mx_wide_supported(a, mode)) t = 1;

@@ -4,7 +4,9 @@
 // MXFP4 routed weights), but each MMA covers N = 256 weight rows instead of 128:
 //   MODE 0 (GEMM-1): gate 128 + up 128 rows, h = silu(x Wg^T) * (x Wu^T) for
 //                    128 columns of h, re-quantised to MXFP8 per 32 along I;
-//   MODE 1 (GEMM-2): 256 rows of W_down, y = h Wd^T for 256 columns, fp32.
+//   MODE 1 (GEMM-2): 256 rows of W_down, y = h Wd^T for 256 columns, fp32,
+//                    staged per warp through shared memory and stored as
+//                    64-byte row segments.
 //
 // What sets the pace of these kernels is how much each issuing thread does
 // per K stage: every tcgen05 instruction, barrier wait and TMA issue costs
@@ -47,7 +49,7 @@
 //   warp 1      TMEM allocator + MMA issuer: 4 MMAs (K = 32) per stage.
 //   warps 3-10  epilogue: warp w reads TMEM lane quarter w % 4 and accumulator
 //               columns 128 * ((w - 3) / 4) .. +127: GEMM-1 h columns 64 of
-//               them, GEMM-2 128 y columns, stored from registers.
+//               them, GEMM-2 128 y columns (through a 2 KB staging block).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -88,8 +90,15 @@ constexpr int wOffA = wStagesB * wBTile;
 constexpr int wOffSf = wOffA + wStagesA * wATile;
 constexpr int wOffTable = wOffSf + wGroupSlots * wGroupBytes;
 constexpr int wOffBars = wOffTable + wTableBytes;
-constexpr int wSmem = 1024 + wOffBars + wBarBytes;
-static_assert(wSmem <= 232448, "shared memory budget");
+// GEMM-2 epilogue staging after the barriers: one 32-row x 16-column fp32 block
+// (2 KB) per epilogue warp.
+constexpr int wStgWarp = 32 * 16;          // floats
+constexpr int wOffStg = wOffBars + wBarBytes;
+template <int MODE>
+constexpr int wSmemFor() { return 1024 + wOffStg + (MODE == 1 ? wEpiWarps * wStgWarp * 4 : 0); }
+constexpr int wSmem = wSmemFor<0>();
+static_assert(wSmemFor<1>() <= 232448, "shared memory budget");
+static_assert(wOffStg % 16 == 0, "16-byte staging stores");
 static_assert(wSfCol0 + 16 * wStagesB <= wTmemCols, "TMEM budget");
 static_assert(wNumBars * 8 + 8 <= wBarBytes, "barrier area");
 static_assert(wStagesA <= wStagesB, "an activation slot is freed by a weight-ring phase no later than its own");
@@ -129,15 +138,6 @@ __device__ __forceinline__ void store_h_block(const uint32_t (&g)[32], const uin
 // (n = 0, 1, ...) when stage n * depth + slot completes.
 __device__ __forceinline__ uint32_t round_parity(int stage, int depth) { return (uint32_t)(stage / depth) & 1u; }
 
-// 32 fp32 values of a y row, as eight 16-byte stores.
-__device__ __forceinline__ void store_y_cols(const uint32_t (&v)[32], float* dst) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    d[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                       __uint_as_float(v[4 * j + 3]));
-}
-
 template <int MODE, bool W4>
 __global__ void __launch_bounds__(wThreads, 1)
     grouped_gemm_mx_wide_kernel(const __grid_constant__ CUtensorMap map_act,
@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(wThreads, 1)
   int32_t* tile_start = reinterpret_cast<int32_t*>(base + wOffTable);
   int32_t* row_start = tile_start + (wMaxGroups + 8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + wOffBars);
+  float* y_stage = reinterpret_cast<float*>(base + wOffStg);  // GEMM-2 only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + wNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -479,13 +480,37 @@ __global__ void __launch_bounds__(wThreads, 1)
       const TileInfo ti = decode_tile_s<128>(p.G, tile_start, row_start, tile);
       const int r = ti.tt * 128 + q * 32 + lane;
       if (MODE == 1) {
-        if (r < ti.nrows) {
-          float* yrow = static_cast<float*>(p.out) + (size_t)(ti.row0 + r) * p.N + ti.wt * kCols + hh * 128;
-          store_y_cols(g0, yrow);
-          store_y_cols(g1, yrow + 32);
-          store_y_cols(u0, yrow + 64);
-          store_y_cols(u1, yrow + 96);
-        }
+        // y leaves through this warp's 2 KB staging block, 16 columns at a
+        // time: each lane writes its row's four 16-byte chunks (chunk c of row
+        // i at position c ^ ((i >> 1) & 3), so neither side has bank
+        // conflicts), then every store instruction writes eight rows' 64-byte
+        // segments (four lanes a row) instead of 16 bytes in each of 32 rows.
+        float* stg = y_stage + (warp - wEpiWarp0) * wStgWarp;
+        const int r0 = ti.tt * 128 + q * 32;  // this warp's first row within the group
+        float* ycol = static_cast<float*>(p.out) + (size_t)ti.row0 * p.N + ti.wt * kCols + hh * 128;
+        auto put = [&](const uint32_t (&v)[32], int c0) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<float4*>(stg + lane * 16 + ((c ^ ((lane >> 1) & 3)) << 2)) =
+                  make_float4(__uint_as_float(v[16 * b + 4 * c]), __uint_as_float(v[16 * b + 4 * c + 1]),
+                              __uint_as_float(v[16 * b + 4 * c + 2]), __uint_as_float(v[16 * b + 4 * c + 3]));
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i = (lane >> 2) + 8 * k, c = lane & 3;
+              const float4 val = *reinterpret_cast<const float4*>(stg + i * 16 + ((c ^ ((i >> 1) & 3)) << 2));
+              if (r0 + i < ti.nrows)
+                *reinterpret_cast<float4*>(ycol + (size_t)(r0 + i) * p.N + c0 + 16 * b + 4 * c) = val;
+            }
+            __syncwarp();
+          }
+        };
+        put(g0, 0);
+        put(g1, 32);
+        put(u0, 64);
+        put(u1, 96);
       } else if (r < ti.nrows) {
         const long long a_blk = tile_start[ti.g] / n_wt + ti.tt;
         uint8_t* h_atoms = p.out_scale + a_blk * (p.N / 128) * kAtomBytes;
@@ -545,7 +570,7 @@ cudaError_t run_gemm_mx_wide(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long n_wt = N / (MODE == 0 ? 128 : 256);
   const long long max_tiles = n_wt * ((a.rows + 127) / 128 + G);
   const int grid = (int)(max_tiles < a.num_sms ? max_tiles : a.num_sms);
-  grouped_gemm_mx_wide_kernel<MODE, W4><<<grid, wThreads, wSmem, s>>>(m_act, m_w0, m_w1, p);
+  grouped_gemm_mx_wide_kernel<MODE, W4><<<grid, wThreads, wSmemFor<MODE>(), s>>>(m_act, m_w0, m_w1, p);
   return cudaGetLastError();
 }
 
@@ -559,8 +584,10 @@ cudaError_t gemm_mx_wide_prepare_device() {
   const cudaError_t errs[] = {
       cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
       cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
-      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem),
-      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wSmem)};
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           wSmemFor<1>()),
+      cudaFuncSetAttribute(grouped_gemm_mx_wide_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           wSmemFor<1>())};
   for (cudaError_t e : errs)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
